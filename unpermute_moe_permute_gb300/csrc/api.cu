@@ -1,0 +1,151 @@
+// C-ABI glue: status strings, device status readback, argument checks and
+// dtype dispatch of the expert-MLP GEMMs.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+int launch_gmm_f32(bool swiglu, const float* A, const float* B0, const float* B1,
+                   const int32_t* off, int N, int Kd, int Nout, int E, float* out, float* save,
+                   cudaStream_t s);
+int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const int32_t* off,
+                            int N, int H, int I, int E, void* act, void* save, int32_t* status,
+                            cudaStream_t s);
+int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int N, int H, int I,
+                         int E, void* out, int32_t* status, cudaStream_t s);
+int launch_mlp_grad_bf16(const void* dY, const void* X, const void* act, const void* gate_up,
+                         const int32_t* off, int N, int H, int I, int E, const void* Wg,
+                         const void* Wu, const void* Wd, void* dgu, void* dX, void* dWg,
+                         void* dWu, void* dWd, int32_t* status, cudaStream_t s);
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+int check_mlp(const void* A, int dtype, const int32_t* off, int N, int H, int I, int E) {
+  if (N < 0 || H <= 0 || I <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts) return MOE_ERR_SHAPE;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (!off || (N > 0 && !A)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_F32 && (H % 4 || I % 4)) return MOE_ERR_SHAPE;
+  if (dtype == MOE_BF16 && (H % 64 || I % 64)) return MOE_ERR_SHAPE;
+  if ((long long)N * (2LL * I > H ? 2LL * I : H) > (1LL << 40)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dtype, shape or device";
+    case MOE_ERR_CAPACITY: return "output capacity exceeded";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_BAD_ID: return "expert id out of range or repeated in a row";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int moe_abi_version(void) { return 1; }
+
+extern "C" int moe_check_status(const int32_t* dev_status, cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (dev_status == nullptr) return MOE_OK;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return v;
+}
+
+extern "C" int moe_gate_up_swiglu(const void* permuted, int dtype, const int32_t* expert_offsets,
+                                  int N, int H, int I, int E, const void* W_gate,
+                                  const void* W_up, void* act, void* gate_up_save,
+                                  int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_mlp(permuted, dtype, expert_offsets, N, H, I, E);
+  if (rc) return rc;
+  if (N == 0) return MOE_OK;
+  if (!W_gate || !W_up || !act) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {permuted, W_gate, W_up, act, gate_up_save};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_F32)
+    return launch_gmm_f32(true, static_cast<const float*>(permuted),
+                          static_cast<const float*>(W_gate), static_cast<const float*>(W_up),
+                          expert_offsets, N, H, I, E, static_cast<float*>(act),
+                          static_cast<float*>(gate_up_save), stream);
+  return launch_gmm_bf16_gate_up(permuted, W_gate, W_up, expert_offsets, N, H, I, E, act,
+                                 gate_up_save, dev_status, stream);
+}
+
+extern "C" int moe_down_proj(const void* act, int dtype, const int32_t* expert_offsets, int N,
+                             int H, int I, int E, const void* W_down, void* expanded,
+                             int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_mlp(act, dtype, expert_offsets, N, H, I, E);
+  if (rc) return rc;
+  if (N == 0) return MOE_OK;
+  if (!W_down || !expanded) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {act, W_down, expanded};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_F32)
+    return launch_gmm_f32(false, static_cast<const float*>(act),
+                          static_cast<const float*>(W_down), nullptr, expert_offsets, N, I, H, E,
+                          static_cast<float*>(expanded), nullptr, stream);
+  return launch_gmm_bf16_down(act, W_down, expert_offsets, N, H, I, E, expanded, dev_status,
+                              stream);
+}
+
+extern "C" int moe_expert_mlp(const void* permuted, int dtype, const int32_t* expert_offsets,
+                              int N, int H, int I, int E, const void* W_gate, const void* W_up,
+                              const void* W_down, void* act, void* expanded, void* gate_up_save,
+                              int32_t* dev_status, cudaStream_t stream) {
+  int rc = moe_gate_up_swiglu(permuted, dtype, expert_offsets, N, H, I, E, W_gate, W_up, act,
+                              gate_up_save, dev_status, stream);
+  if (rc) return rc;
+  return moe_down_proj(act, dtype, expert_offsets, N, H, I, E, W_down, expanded, dev_status,
+                       stream);
+}
+
+extern "C" int moe_expert_mlp_grad(const void* grad_expanded, const void* permuted,
+                                   const void* act, const void* gate_up_save, int dtype,
+                                   const int32_t* expert_offsets, int N, int H, int I, int E,
+                                   const void* W_gate, const void* W_up, const void* W_down,
+                                   void* dgu, void* d_permuted, void* dW_gate, void* dW_up,
+                                   void* dW_down, int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_mlp(grad_expanded, dtype, expert_offsets, N, H, I, E);
+  if (rc) return rc;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!W_gate || !W_up || !W_down || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (!permuted || !act || !gate_up_save || !dgu || !d_permuted))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {grad_expanded, permuted, act,     gate_up_save, W_gate, W_up,
+                        W_down,        dgu,      d_permuted, dW_gate,    dW_up,  dW_down};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return launch_mlp_grad_bf16(grad_expanded, permuted, act, gate_up_save, expert_offsets, N, H, I,
+                              E, W_gate, W_up, W_down, dgu, d_permuted, dW_gate, dW_up, dW_down,
+                              dev_status, stream);
+}

@@ -1,0 +1,133 @@
+// Rank-major -> expert-major permute indices (hyper_parallel
+// expert_parallel.py, _generate_permute_indices).
+//
+// counts[r*E + e] rows arrived from rank r for local expert e, stored
+// rank-major: [r0.e0 | r0.e1 | ... | r1.e0 | ...].  The expert-major buffer
+// visits the same blocks as [e0.r0 | e0.r1 | ... | e1.r0 | ...].  Destination
+// i inside block (e, r) at offset j reads source start_rm(r, e) + j.
+//
+// One launch, no host round trip (the page drains `total` to the host before
+// building the indices; here it stays on the device).  Every CTA stages the
+// R*E counts in shared memory and computes both exclusive scans (rank-major
+// source starts, expert-major destination starts), then the CTAs split the
+// blocks between them and each warp writes one block's run of indices.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kIdxThreads = 1024;
+constexpr int kMaxBlocks = 2048;  // R * E (combine_v2 constraints: local experts x EP size <= 2048)
+
+// Exclusive scan of n values in smem (in place) by one CTA of kIdxThreads.
+// Each thread scans a contiguous run serially, then the run totals are
+// scanned across the CTA.
+__device__ void cta_exclusive_scan(int32_t* a, int n, int32_t* tmp /* >= 32 */,
+                                   int32_t* total_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + kIdxThreads - 1) / kIdxThreads;
+  const int lo = min(tid * per, n), hi = min(lo + per, n);
+  int s = 0;
+  for (int i = lo; i < hi; ++i) s += a[i];
+  int incl = s;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = tmp[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    tmp[lane] = w;
+  }
+  __syncthreads();
+  int run = incl - s + (warp > 0 ? tmp[warp - 1] : 0);
+  for (int i = lo; i < hi; ++i) {
+    const int c = a[i];
+    a[i] = run;
+    run += c;
+  }
+  if (total_out && tid == 0) *total_out = tmp[31];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kIdxThreads)
+permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t* __restrict__ indices,
+                       int capacity, int32_t* __restrict__ tokens_per_expert, int32_t* total,
+                       int32_t* status) {
+  __shared__ int32_t cnt_em[kMaxBlocks];  // counts in (e, r) order
+  __shared__ int32_t src_rm[kMaxBlocks];  // rank-major source starts, (r, e) order
+  __shared__ int32_t dst_em[kMaxBlocks];  // expert-major destination starts, (e, r) order
+  __shared__ int32_t tmp[32];
+  __shared__ int32_t s_total;
+  __shared__ int32_t s_bad;
+  const int nb = R * E;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < nb; b += kIdxThreads) {
+    const int r = b / E, e = b - r * E;
+    int c = counts[b];
+    if (c < 0) {
+      s_bad = 1;
+      c = 0;
+    }
+    src_rm[b] = c;
+    cnt_em[e * R + r] = c;
+    dst_em[e * R + r] = c;
+  }
+  __syncthreads();
+  cta_exclusive_scan(src_rm, nb, tmp, nullptr);
+  cta_exclusive_scan(dst_em, nb, tmp, &s_total);
+  const int tot = s_total;
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += kIdxThreads) {
+      int s = 0;
+      for (int r = 0; r < R; ++r) s += cnt_em[e * R + r];
+      tokens_per_expert[e] = s;
+    }
+    if (threadIdx.x == 0) {
+      *total = tot;
+      if (s_bad) set_status(status, MOE_ERR_INVALID_ARG);
+      if (tot > capacity) set_status(status, MOE_ERR_CAPACITY);
+    }
+  }
+  if (tot > capacity) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = kIdxThreads / 32;
+  for (int b = blockIdx.x * nwarps + warp; b < nb; b += gridDim.x * nwarps) {
+    const int e = b / R, r = b - e * R;  // expert-major block (e, r)
+    const int c = cnt_em[b];
+    const int src = src_rm[r * E + e];
+    const int dst = dst_em[b];
+    for (int j = lane; j < c; j += 32) indices[dst + j] = src + j;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_permute_indices(const int32_t* counts, int R, int E, int32_t* indices,
+                                   int capacity, int32_t* tokens_per_expert, int32_t* total,
+                                   int32_t* dev_status, cudaStream_t stream) {
+  if (R <= 0 || E <= 0 || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if ((long long)R * E > kMaxBlocks) return MOE_ERR_SHAPE;
+  if (!counts || !tokens_per_expert || !total || (capacity > 0 && !indices))
+    return MOE_ERR_INVALID_ARG;
+  // Enough CTAs that each warp writes about one (e, r) block; at most one
+  // wave of the GPU.
+  const int nb = R * E;
+  int grid = (nb + 31) / 32;
+  grid = max(1, min(grid, sm_count()));
+  permute_indices_kernel<<<grid, kIdxThreads, 0, stream>>>(counts, R, E, indices, capacity,
+                                                           tokens_per_expert, total, dev_status);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}

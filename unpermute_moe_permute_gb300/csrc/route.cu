@@ -1,0 +1,284 @@
+// Token permute for the MoE expert layer: expert histogram, scan, stable
+// expert-major rank, row copy.  Also the inverse of sorted_indices.
+//
+// Layout (hyper_parallel expert_parallel.py, _generate_permute_indices
+// docstring): the permuted buffer holds all rows routed to expert 0, then all
+// rows of expert 1, ...; inside one expert the rows keep increasing flat slot
+// order f = t*K + k.  sorted_indices uses the gather convention of that
+// page's permuted_indices: entry i is the slot whose row lands at row i.
+//
+// Design: three small kernels over int32 ids (about 4 bytes per slot each)
+// and one bandwidth kernel that reads every token row once and writes it to
+// its K destinations with 16-byte vectors.  The rank pass is deterministic:
+// per-block counts -> per-(block, expert) bases -> per-warp bases -> in-warp
+// rank from __match_any_sync peers, so no atomic ordering reaches the output.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kSlotsPerWarp = 256;
+constexpr int kChunk = kRouteWarps * kSlotsPerWarp;  // slots per block
+
+// Expert a slot is dispatched to, or -1: ids outside [0, E_total) and ids
+// repeated earlier in the same row are not dispatched (and are errors);
+// special ids in [E, E_total) are legal but not dispatched.
+__device__ __forceinline__ int slot_expert(const int32_t* __restrict__ ids, int f, int K, int E,
+                                           int E_total, bool* bad) {
+  const int id = ids[f];
+  const int row0 = (f / K) * K;
+  bool ok = (id >= 0) && (id < E_total);
+  for (int j = row0; j < f; ++j) ok = ok && (ids[j] != id);
+  *bad = !ok;
+  return (ok && id < E) ? id : -1;
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+route_hist_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total,
+                  int32_t* __restrict__ blk_counts, int32_t* status) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kChunk;
+  const int end = min(base + kChunk, TK);
+  bool any_bad = false;
+  for (int f = base + threadIdx.x; f < end; f += kRouteThreads) {
+    bool bad;
+    const int e = slot_expert(ids, f, K, E, E_total, &bad);
+    any_bad |= bad;
+    if (e >= 0) atomicAdd(&hist[e], 1);
+  }
+  if (any_bad) set_status(status, MOE_ERR_BAD_ID);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kRouteThreads)
+    blk_counts[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One block of 1024 threads: thread e owns expert e (E <= 1024).
+// In place: blk_counts[b][e] becomes the first permuted row of block b's
+// slots of expert e.
+__global__ void __launch_bounds__(1024)
+route_scan_kernel(int32_t* __restrict__ blk, int nblk, int E, int32_t* __restrict__ tokens_per_expert,
+                  int32_t* __restrict__ expert_offsets) {
+  __shared__ int32_t warp_tot[32];
+  const int e = threadIdx.x;
+  const int lane = e & 31, warp = e >> 5;
+  int cnt = 0;
+  if (e < E)
+    for (int b = 0; b < nblk; ++b) cnt += blk[(size_t)b * E + e];
+  // block-wide exclusive scan of cnt
+  int incl = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    warp_tot[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
+  if (e < E) {
+    tokens_per_expert[e] = cnt;
+    expert_offsets[e] = excl;
+    if (e == E - 1) expert_offsets[E] = excl + cnt;
+    int run = excl;
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blk[(size_t)b * E + e];
+      blk[(size_t)b * E + e] = run;
+      run += c;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total,
+                     const int32_t* __restrict__ blk_base, int32_t* __restrict__ sorted_indices,
+                     int32_t* __restrict__ row_map) {
+  extern __shared__ int32_t cnt[];  // [kRouteWarps][E]
+  for (int i = threadIdx.x; i < kRouteWarps * E; i += kRouteThreads) cnt[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wbase = blockIdx.x * kChunk + warp * kSlotsPerWarp;
+  int32_t* my = cnt + warp * E;
+  // 1. per-warp counts
+  for (int i = 0; i < kSlotsPerWarp; i += 32) {
+    const int f = wbase + i + lane;
+    if (f < TK) {
+      bool bad;
+      const int e = slot_expert(ids, f, K, E, E_total, &bad);
+      if (e >= 0) atomicAdd(&my[e], 1);
+    }
+  }
+  __syncthreads();
+  // 2. per-warp bases: block base of the expert + counts of earlier warps
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+    int run = blk_base[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // 3. stable rank inside each 32-slot step: peers with the same expert and a
+  //    lower lane come first; the step's leader advances the warp's base.
+  for (int i = 0; i < kSlotsPerWarp; i += 32) {
+    const int f = wbase + i + lane;
+    int e = -1;
+    if (f < TK) {
+      bool bad;
+      e = slot_expert(ids, f, K, E, E_total, &bad);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lanemask_lt());
+    if (e >= 0) {
+      const int pos = my[e] + rank;
+      sorted_indices[pos] = f;
+      row_map[f] = pos;
+    } else if (f < TK) {
+      row_map[f] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// One warp per token: read the row once (16-byte vectors), write it to each
+// of its K permuted rows.
+template <int kUnroll>
+__global__ void __launch_bounds__(256)
+permute_rows_kernel(const uint8_t* __restrict__ tokens, const int32_t* __restrict__ row_map, int T,
+                    int K, int row_bytes, uint8_t* __restrict__ permuted) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const int my_rm = lane < K ? row_map[(size_t)t * K + lane] : -1;
+  const int nvec = row_bytes >> 4;
+  const uint8_t* src = tokens + (size_t)t * row_bytes;
+  // The trip count is the same for every lane (the shuffles below need the
+  // whole warp); lanes past the row end only skip their loads and stores.
+  for (int base = 0; base < nvec; base += 32 * kUnroll) {
+    const int v0 = base + lane;
+    uint4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = v0 + u * 32;
+      if (v < nvec) x[u] = ld_nc_v4(src + ((size_t)v << 4));
+    }
+    for (int k = 0; k < K; ++k) {
+      const int r = __shfl_sync(0xffffffffu, my_rm, k);
+      if (r < 0) continue;
+      uint8_t* dst = permuted + (size_t)r * row_bytes;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + u * 32;
+        if (v < nvec) st_v4(dst + ((size_t)v << 4), x[u]);
+      }
+    }
+  }
+}
+
+__global__ void fill_kernel(int32_t* __restrict__ p, int n, int32_t value) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    p[i] = value;
+}
+
+__global__ void invert_kernel(const int32_t* __restrict__ sorted_indices, int N, int TK,
+                              int32_t* __restrict__ row_map) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x) {
+    const int f = sorted_indices[i];
+    if (f >= 0 && f < TK) row_map[f] = i;
+  }
+}
+
+}  // namespace
+
+// ---- host entry points -------------------------------------------------------
+
+static inline int route_blocks(int TK) { return (TK + kChunk - 1) / kChunk; }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
+  if (T < 0 || K <= 0 || E <= 0) return 0;
+  const long long TK = (long long)T * K;
+  const long long nblk = (TK + kChunk - 1) / kChunk;
+  return (size_t)((nblk > 0 ? nblk : 1) * E * sizeof(int32_t));
+}
+
+extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T, int H,
+                           int K, int E, int num_special, void* permuted, int32_t* sorted_indices,
+                           int32_t* row_map, int32_t* tokens_per_expert, int32_t* expert_offsets,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           cudaStream_t stream) {
+  if (T < 0 || H <= 0 || K <= 0 || E <= 0 || num_special < 0) return MOE_ERR_INVALID_ARG;
+  if (K > kMaxK || E > kMaxExperts || (long long)K > (long long)E + num_special)
+    return MOE_ERR_SHAPE;
+  if ((long long)T * K > 0x7fffffffLL || (long long)E + num_special > 0x7fffffffLL)
+    return MOE_ERR_SHAPE;
+  if (tokens != nullptr) {
+    const int esz = dtype_size(dtype);
+    if (esz == 0) return MOE_ERR_INVALID_ARG;
+    if (permuted == nullptr) return MOE_ERR_INVALID_ARG;
+    if (((size_t)H * esz) % 16 != 0) return MOE_ERR_SHAPE;
+    if (!aligned16(tokens) || !aligned16(permuted)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!tokens_per_expert || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  const int TK = T * K;
+  if (TK > 0 && (!expert_ids || !sorted_indices || !row_map)) return MOE_ERR_INVALID_ARG;
+  const int nblk = route_blocks(TK);
+  if (TK > 0 && (workspace == nullptr || workspace_bytes < moe_permute_workspace_size(T, K, E)))
+    return MOE_ERR_INVALID_ARG;
+  if (TK == 0) {
+    // Nothing routed: zero counts, zero offsets.
+    fill_kernel<<<1, 256, 0, stream>>>(tokens_per_expert, E, 0);
+    fill_kernel<<<1, 256, 0, stream>>>(expert_offsets, E + 1, 0);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+  }
+  int32_t* blk = static_cast<int32_t*>(workspace);
+  const int E_total = E + num_special;
+  route_hist_kernel<<<nblk, kRouteThreads, E * sizeof(int32_t), stream>>>(expert_ids, TK, K, E,
+                                                                         E_total, blk, dev_status);
+  route_scan_kernel<<<1, 1024, 0, stream>>>(blk, nblk, E, tokens_per_expert, expert_offsets);
+  const size_t scatter_smem = (size_t)kRouteWarps * E * sizeof(int32_t);
+  if (scatter_smem > 48 * 1024)
+    cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)scatter_smem);
+  route_scatter_kernel<<<nblk, kRouteThreads, scatter_smem, stream>>>(expert_ids, TK, K, E, E_total,
+                                                                      blk, sorted_indices, row_map);
+  if (tokens != nullptr && T > 0) {
+    const int row_bytes = H * dtype_size(dtype);
+    permute_rows_kernel<4><<<(T + 7) / 8, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(tokens), row_map, T, K, row_bytes,
+        static_cast<uint8_t*>(permuted));
+  }
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+extern "C" int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, int TK,
+                                         int32_t* row_map, cudaStream_t stream) {
+  if (N < 0 || TK < 0 || N > TK) return MOE_ERR_INVALID_ARG;
+  if (TK == 0) return MOE_OK;
+  if (!row_map || (N > 0 && !sorted_indices)) return MOE_ERR_INVALID_ARG;
+  const int grid = min((TK + 255) / 256, 4 * sm_count());
+  fill_kernel<<<grid, 256, 0, stream>>>(row_map, TK, -1);
+  if (N > 0) invert_kernel<<<min((N + 255) / 256, 4 * sm_count()), 256, 0, stream>>>(sorted_indices, N, TK, row_map);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
