@@ -80,6 +80,10 @@ const char* moe_status_string(int status);
 /* ABI version: bumped when a signature changes. */
 int moe_abi_version(void);
 
+/* Number of kernels this library has launched in the process so far (all
+ * devices, all streams).  For tracing and launch accounting. */
+unsigned long long moe_kernel_launches(void);
+
 /* Synchronise `stream`, then read the device status word written by earlier
  * calls.  Returns MOE_OK or the first device-side MOE_ERR_* code, or
  * MOE_ERR_CUDA if the stream reported an error.  Does not reset the word. */

@@ -51,6 +51,7 @@ _SZ = ctypes.c_size_t
 _SIGNATURES = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_abi_version": ([], _I),
+    "moe_kernel_launches": ([], ctypes.c_ulonglong),
     "moe_check_status": ([_P, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
     "moe_permute": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
@@ -134,6 +135,11 @@ def _check(t: Optional[torch.Tensor], dtype, name: str):
 def new_status(device=None) -> torch.Tensor:
     """A zeroed device status word for the dev_status arguments."""
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def moe_kernel_launches() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(load_library().moe_kernel_launches())
 
 
 def moe_check_status(dev_status: Optional[torch.Tensor]) -> int:

@@ -1,6 +1,6 @@
 // C-ABI glue: status strings, device status readback, argument checks and
 // dtype dispatch of the expert-MLP GEMMs.
-#include <mutex>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -18,6 +18,10 @@ int launch_mlp_grad_bf16(const void* dY, const void* X, const void* act, const v
                          const int32_t* off, int N, int H, int I, int E, const void* Wg,
                          const void* Wu, const void* Wd, void* dgu, void* dX, void* dWg,
                          void* dWu, void* dWd, int32_t* status, cudaStream_t s);
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 int sm_count() {
   static int cached[64] = {0};
@@ -65,6 +69,10 @@ extern "C" const char* moe_status_string(int status) {
 }
 
 extern "C" int moe_abi_version(void) { return 1; }
+
+extern "C" unsigned long long moe_kernel_launches(void) {
+  return g_launches.load(std::memory_order_relaxed);
+}
 
 extern "C" int moe_check_status(const int32_t* dev_status, cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) {

@@ -106,6 +106,11 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     }                                                        \
   } while (0)
 
+// Launch accounting: every host entry point adds the kernels it launched.
+namespace moe {
+void count_launches(int n);
+}
+
 namespace moe {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

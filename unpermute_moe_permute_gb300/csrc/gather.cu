@@ -234,6 +234,7 @@ void launch_unpermute(const void* Y, const int32_t* rm, const float* p, int Tn, 
                       void* out, cudaStream_t s) {
   unpermute_kernel<T, KMAX><<<(Tn + kWarpsPerBlock - 1) / kWarpsPerBlock, 256, 0, s>>>(
       static_cast<const T*>(Y), rm, p, Tn, H, K, N, static_cast<T*>(out));
+  count_launches(1);
 }
 
 template <typename T, int KMAX>
@@ -242,6 +243,7 @@ void launch_unpermute_grad(const void* g, const void* X, const int32_t* rm, cons
   unpermute_grad_kernel<T, KMAX><<<(Tn + kWarpsPerBlock - 1) / kWarpsPerBlock, 256, 0, s>>>(
       static_cast<const T*>(g), static_cast<const T*>(X), rm, p, Tn, H, K, N, static_cast<T*>(gp),
       gprobs);
+  count_launches(1);
 }
 
 template <typename T, int KMAX>
@@ -253,6 +255,7 @@ void launch_combine(const void* Y, const int32_t* rm, const int32_t* ids, const 
       static_cast<const T*>(Y), rm, ids, sc, static_cast<const T*>(sh),
       static_cast<const T*>(ori), Tn, H, K, N, E, Z, C, Cn, static_cast<const T*>(a1),
       static_cast<const T*>(a2), static_cast<const T*>(cv), static_cast<T*>(out), st);
+  count_launches(1);
 }
 
 // Pick the smallest compiled K bound that covers K (keeps the per-slot

@@ -125,6 +125,7 @@ int launch_gmm_f32(bool swiglu, const float* A, const float* B0, const float* B1
     gmm_f32_kernel<true><<<grid, kThreads, 0, s>>>(A, B0, B1, off, N, Kd, Nout, E, out, save);
   else
     gmm_f32_kernel<false><<<grid, kThreads, 0, s>>>(A, B0, nullptr, off, N, Kd, Nout, E, out, nullptr);
+  count_launches(1);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

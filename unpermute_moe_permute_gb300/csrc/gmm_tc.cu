@@ -1,20 +1,651 @@
-// bf16 grouped GEMMs on tcgen05 tensor cores (placeholder until the kernels land).
+// bf16 grouped GEMMs of the expert MLP on tcgen05 tensor cores (sm_103a).
+//
+// The per-expert loop of the expert MLP, replaced by one grouped matmul per
+// projection with SwiGLU fused in (twinkle PR "NPU EP experts forward uses
+// NPU grouped matmul"), written for Blackwell:
+//
+//   * one persistent CTA per SM walks a static round-robin list of
+//     (expert, m-tile, n-tile) tiles computed on the device from the expert
+//     row offsets (no host sync, empty experts have no tiles);
+//   * warp 0 issues TMA loads of 128x64 A and 256x64 B bf16 tiles (128-byte
+//     swizzle) into a 4-stage shared-memory ring;
+//   * warp 1 allocates 512 tensor-memory columns (two 128x256 fp32
+//     accumulators) and one thread issues tcgen05.mma (M=128, N=256, K=16);
+//   * warps 2-5 drain an accumulator with tcgen05.ld while the next tile
+//     accumulates into the other one, apply the epilogue and store bf16.
+//
+// Six variants (KIND) share the machinery:
+//   FwdGateUp   act = silu(X Wg^T) * (X Wu^T)       B tile = 128 rows of Wg
+//                                                   + 128 rows of Wu
+//   FwdDown     expanded = act Wd^T
+//   DgradDown   dA = dY Wd, then the SwiGLU backward -> dgu = (dg, du)
+//   DgradGateUp dX = dg Wg + du Wu  (one K loop over [dg | du] x [Wg ; Wu])
+//   WgradDown   dWd[e] = dY_e^T act_e               (K = the expert's rows)
+//   WgradGateUp [dWg; dWu][e] = dgu_e^T X_e
+// Forward operands are K-major.  In the backward the weight operand of the
+// dgrads and both operands of the wgrads are MN-major (contiguous along the
+// output dimension), which UMMA reads directly from 64-element-wide
+// swizzled TMA boxes, so no transposed copy of any tensor is made.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
+#include "sched.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
+namespace tc {
 
-int launch_gmm_bf16_gate_up(const void*, const void*, const void*, const int32_t*, int, int, int,
-                            int, void*, void*, int32_t*, cudaStream_t) {
-  return MOE_ERR_UNSUPPORTED;
+constexpr int BM = 128, BN = 256, BK = 64, UK = 16, STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;        // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;   // one 64 (M/N) x 64 (K) box, 8 KB
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t CTRL_BYTES = 128 + (kMaxExperts + 1) * 4 + 32 * 4;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + CTRL_BYTES + 1024;
+
+enum Kind : int {
+  kFwdGateUp = 0,
+  kFwdDown = 1,
+  kDgradDown = 2,
+  kDgradGateUp = 3,
+  kWgradDown = 4,
+  kWgradGateUp = 5,
+};
+
+template <int KIND>
+struct Traits {
+  static constexpr bool a_mn = (KIND == kWgradDown || KIND == kWgradGateUp);
+  static constexpr bool b_mn = (KIND >= kDgradDown);
+  static constexpr bool wgrad = (KIND == kWgradDown || KIND == kWgradGateUp);
+  static constexpr int n_per_tile = (KIND == kFwdGateUp) ? 128 : 256;  // output columns
+  static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
+};
+
+struct Params {
+  const int32_t* off;
+  int N;        // row capacity of the token-major buffers
+  int E;
+  int Kd;       // reduction length of the row-tiled kinds
+  int I;        // expert intermediate size
+  int Nout;     // output columns
+  int Mout;     // output rows per expert (wgrad)
+  int n_tiles;  // tiles along the output columns
+  int m_tiles;  // tiles along the output rows per expert (wgrad)
+  __nv_bfloat16* out;
+  __nv_bfloat16* out2;
+  __nv_bfloat16* save;
+  const __nv_bfloat16* aux;
+  int32_t* status;
+};
+
+struct Tile {
+  int e, lo, hi;  // expert and its row range
+  int m0, n0;     // first output row / column of the tile
+  int kblocks;    // 64-deep k blocks
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_t* prefix) {
+  Tile x;
+  if constexpr (!Traits<KIND>::wgrad) {
+    const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
+    const int e = find_expert(prefix, p.E, mt);
+    const ExpertRows r = expert_rows(p.off, e, p.N);
+    x.e = e;
+    x.lo = r.lo;
+    x.hi = r.hi;
+    x.m0 = r.lo + (mt - prefix[e]) * BM;
+    x.n0 = nt * Traits<KIND>::n_per_tile;
+    x.kblocks = p.Kd / BK;
+  } else {
+    const int per = p.m_tiles * p.n_tiles;
+    const int e = t / per, rem = t - e * per;
+    const int mt = rem / p.n_tiles, nt = rem - mt * p.n_tiles;
+    const ExpertRows r = expert_rows(p.off, e, p.N);
+    x.e = e;
+    x.lo = r.lo;
+    x.hi = r.hi;
+    x.m0 = mt * BM;
+    x.n0 = nt * BN;
+    x.kblocks = (r.hi - r.lo + BK - 1) / BK;
+  }
+  return x;
 }
-int launch_gmm_bf16_down(const void*, const void*, const int32_t*, int, int, int, int, void*,
-                         int32_t*, cudaStream_t) {
-  return MOE_ERR_UNSUPPORTED;
+
+// TMA loads of k block kb of tile x into one stage.
+template <int KIND>
+__device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& p, uint32_t sa,
+                                           uint32_t sb, uint32_t bar, const CUtensorMap* mA,
+                                           const CUtensorMap* mB0, const CUtensorMap* mB1) {
+  const int k0 = kb * BK;
+  if constexpr (KIND == kFwdGateUp) {
+    tma_load_2d(sa, mA, bar, k0, x.m0);
+    tma_load_3d(sb, mB0, bar, k0, x.n0, x.e);
+    tma_load_3d(sb + B_BYTES / 2, mB1, bar, k0, x.n0, x.e);
+  } else if constexpr (KIND == kFwdDown) {
+    tma_load_2d(sa, mA, bar, k0, x.m0);
+    tma_load_3d(sb, mB0, bar, k0, x.n0, x.e);
+    tma_load_3d(sb + B_BYTES / 2, mB0, bar, k0, x.n0 + 128, x.e);
+  } else if constexpr (KIND == kDgradDown) {
+    tma_load_2d(sa, mA, bar, k0, x.m0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * MN_BOX_BYTES, mB0, bar, x.n0 + j * 64, k0, x.e);
+  } else if constexpr (KIND == kDgradGateUp) {
+    tma_load_2d(sa, mA, bar, k0, x.m0);
+    const bool up = k0 >= p.I;
+    const int kk = up ? k0 - p.I : k0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      tma_load_3d(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, bar, x.n0 + j * 64, kk, x.e);
+  } else {  // wgrad: both operands MN-major, k = token rows of the expert
+    const int row = x.lo + k0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * MN_BOX_BYTES, mA, bar, x.m0 + j * 64, row);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * MN_BOX_BYTES, mB0, bar, x.n0 + j * 64, row);
+  }
 }
-int launch_mlp_grad_bf16(const void*, const void*, const void*, const void*, const int32_t*, int,
-                         int, int, int, const void*, const void*, const void*, void*, void*,
-                         void*, void*, void*, int32_t*, cudaStream_t) {
-  return MOE_ERR_UNSUPPORTED;
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Store 32 fp32 values (bit patterns) as 32 bf16 = 64 contiguous bytes.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+__device__ __forceinline__ void store_zero32(__nv_bfloat16* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[q] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&f)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = s[q];
+    f[8 * q + 0] = bf_lo(v.x);
+    f[8 * q + 1] = bf_hi(v.x);
+    f[8 * q + 2] = bf_lo(v.y);
+    f[8 * q + 3] = bf_hi(v.y);
+    f[8 * q + 4] = bf_lo(v.z);
+    f[8 * q + 5] = bf_hi(v.z);
+    f[8 * q + 6] = bf_lo(v.w);
+    f[8 * q + 7] = bf_hi(v.w);
+  }
+}
+
+// Epilogue of one tile for one thread: TMEM lane = output row of the tile.
+template <int KIND>
+__device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_t tacc, int lrow) {
+  if constexpr (KIND == kFwdGateUp) {
+    const int row = x.m0 + lrow;
+    const bool ok = row < x.hi;
+    const int I = p.Nout;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t g[32], u[32];
+      tmem_ld_32x32b_x32(tacc + c * 32, g);
+      tmem_ld_32x32b_x32(tacc + 128 + c * 32, u);
+      tmem_ld_wait();
+      const int col = x.n0 + c * 32;
+      if (ok && col < I) {
+        uint32_t a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+          a[j] = __float_as_uint(gv / (1.f + __expf(-gv)) * uv);
+        }
+        store_row32(p.out + (size_t)row * I + col, a);
+        if (p.save != nullptr) {
+          store_row32(p.save + (size_t)row * 2 * I + col, g);
+          store_row32(p.save + (size_t)row * 2 * I + I + col, u);
+        }
+      }
+    }
+  } else if constexpr (KIND == kFwdDown || KIND == kDgradGateUp) {
+    const int row = x.m0 + lrow;
+    const bool ok = row < x.hi;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tacc + c * 32, v);
+      tmem_ld_wait();
+      const int col = x.n0 + c * 32;
+      if (ok && col < p.Nout) store_row32(p.out + (size_t)row * p.Nout + col, v);
+    }
+  } else if constexpr (KIND == kDgradDown) {
+    // dA -> SwiGLU backward with the saved pre-activations (g, u):
+    //   dg = dA * u * s * (1 + g (1 - s)),  du = dA * g * s,  s = sigmoid(g)
+    const int row = x.m0 + lrow;
+    const bool ok = row < x.hi;
+    const int I = p.I;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tacc + c * 32, v);
+      tmem_ld_wait();
+      const int col = x.n0 + c * 32;
+      if (ok && col < I) {
+        float g[32], u[32];
+        load_row32(p.aux + (size_t)row * 2 * I + col, g);
+        load_row32(p.aux + (size_t)row * 2 * I + I + col, u);
+        uint32_t dg[32], du[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float da = __uint_as_float(v[j]);
+          const float s = 1.f / (1.f + __expf(-g[j]));
+          dg[j] = __float_as_uint(da * u[j] * s * (1.f + g[j] * (1.f - s)));
+          du[j] = __float_as_uint(da * g[j] * s);
+        }
+        store_row32(p.out + (size_t)row * 2 * I + col, dg);
+        store_row32(p.out + (size_t)row * 2 * I + I + col, du);
+      }
+    }
+  } else {  // wgrad
+    const int m = x.m0 + lrow;
+    const bool ok = m < p.Mout;
+    __nv_bfloat16* dst_row = nullptr;
+    if (ok) {
+      if constexpr (KIND == kWgradDown) {
+        dst_row = p.out + ((size_t)x.e * p.Mout + m) * p.Nout;
+      } else {
+        dst_row = (m < p.I) ? p.out + ((size_t)x.e * p.I + m) * p.Nout
+                            : p.out2 + ((size_t)x.e * p.I + (m - p.I)) * p.Nout;
+      }
+    }
+    const bool empty = x.kblocks == 0;  // uniform over the tile
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const int col = x.n0 + c * 32;
+      if (empty) {
+        if (ok && col < p.Nout) store_zero32(dst_row + col);
+      } else {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + c * 32, v);
+        tmem_ld_wait();
+        if (ok && col < p.Nout) store_row32(dst_row + col, v);
+      }
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+              const __grid_constant__ CUtensorMap mapB1, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + STAGES * A_BYTES;
+  const uint32_t ctrl = base + STAGES * STAGE_BYTES;
+  uint8_t* gctrl = gbase + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return ctrl + 8u * s; };
+  auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = ctrl + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gctrl + 104);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 108);
+  int32_t* prefix = reinterpret_cast<int32_t*>(gctrl + 128);
+  int32_t* scratch = prefix + (kMaxExperts + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB0);
+    tma_prefetch_desc(&mapB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  int total;
+  if constexpr (Traits<KIND>::wgrad) {
+    __syncthreads();
+    total = p.E * p.m_tiles * p.n_tiles;
+  } else {
+    build_tile_prefix(p.off, p.E, p.N, BM, prefix, scratch);  // ends with __syncthreads
+    total = prefix[p.E] * p.n_tiles;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+      int g = 0;
+      bool run = true;
+      for (int t = blockIdx.x; run && t < total; t += gridDim.x) {
+        const Tile x = decode_tile<KIND>(t, p, prefix);
+        for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
+            run = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+          load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, full_bar(s), &mapA,
+                           &mapB0, &mapB1);
+          issued[s] = (int)ph;
+        }
+      }
+      // wait for every copy this thread issued before the CTA may exit
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s] >= 0) mbar_wait(full_bar(s), (uint32_t)issued[s], abort_flag, p.status, false);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    int g = 0, it = 0;
+    bool run = true;
+    for (int t = blockIdx.x; run && t < total; t += gridDim.x, ++it) {
+      const Tile x = decode_tile<KIND>(t, p, prefix);
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + acc * BN;
+      for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, abort_flag, p.status))) {
+          run = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
+        int nk = BK / UK;
+        if constexpr (Traits<KIND>::wgrad) {
+          // Last k block of an expert: rows past the expert's end belong to
+          // the next expert.  Skip whole 16-row groups past the end and zero
+          // the rest of the last group in every operand box.
+          const int rem = x.hi - (x.lo + kb * BK);
+          if (rem < BK) {
+            nk = (rem + UK - 1) / UK;
+            const int z0 = rem, z1 = nk * UK, zl = z1 - z0;
+            if (zl > 0) {
+              const int n16 = zl * 6 * 8;  // lines x boxes x 16-byte chunks
+              for (int i = lane; i < n16; i += 32) {
+                const int chunk = i & 7, line = i >> 3;
+                const int box = line / zl, r = z0 + line % zl;
+                const uint32_t addr = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
+                                      r * 128 + chunk * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t ad = Traits<KIND>::a_mn ? desc_sw128(sa + kk * (UK * 128), MN_BOX_BYTES, 1024)
+                                                   : desc_sw128(sa + kk * (UK * 2), 16, 1024);
+            const uint64_t bd = Traits<KIND>::b_mn ? desc_sw128(sb + kk * (UK * 128), MN_BOX_BYTES, 1024)
+                                                   : desc_sw128(sb + kk * (UK * 2), 16, 1024);
+            umma_f16(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+        }
+        __syncwarp();
+      }
+      if (!run) break;
+      if (lane == 0) umma_commit(tfull_bar(acc));
+      __syncwarp();
+    }
+    if (lane == 0) {
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, abort_flag, p.status, false);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int lrow = quarter * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const Tile x = decode_tile<KIND>(t, p, prefix);
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
+      epilogue<KIND>(x, p, tacc, lrow);
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---- host side -----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle; dims innermost first, strides in bytes.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+  uint64_t stride = 2;
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    if (i > 0) gstride[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gdim,
+                        gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int KIND>
+int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
+           cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(gmm_tc_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)SMEM_BYTES);
+  });
+  if (attr != cudaSuccess) return MOE_ERR_CUDA;
+  gmm_tc_kernel<KIND><<<sm_count(), kThreads, SMEM_BYTES, s>>>(a, b0, b1, p);
+  count_launches(1);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+int device_ok() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+Params base_params(const int32_t* off, int N, int E, int32_t* status) {
+  Params p{};
+  p.off = off;
+  p.N = N;
+  p.E = E;
+  p.status = status;
+  return p;
+}
+
+}  // namespace tc
+
+using namespace tc;
+
+int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const int32_t* off,
+                            int N, int H, int I, int E, void* act, void* save, int32_t* status,
+                            cudaStream_t s) {
+  if (int rc = device_ok()) return rc;
+  CUtensorMap ma, mg, mu;
+  const uint64_t da[2] = {(uint64_t)H, (uint64_t)N};
+  const uint32_t ba[2] = {64, 128};
+  const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)E};
+  const uint32_t bw[3] = {64, 128, 1};
+  if (!make_map(&ma, A, 2, da, ba) || !make_map(&mg, Wg, 3, dw, bw) || !make_map(&mu, Wu, 3, dw, bw))
+    return MOE_ERR_CUDA;
+  Params p = base_params(off, N, E, status);
+  p.Kd = H;
+  p.I = I;
+  p.Nout = I;
+  p.n_tiles = (I + 127) / 128;
+  p.out = static_cast<__nv_bfloat16*>(act);
+  p.save = static_cast<__nv_bfloat16*>(save);
+  return launch<kFwdGateUp>(ma, mg, mu, p, s);
+}
+
+int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int N, int H, int I,
+                         int E, void* out, int32_t* status, cudaStream_t s) {
+  if (int rc = device_ok()) return rc;
+  CUtensorMap ma, md;
+  const uint64_t da[2] = {(uint64_t)I, (uint64_t)N};
+  const uint32_t ba[2] = {64, 128};
+  const uint64_t dw[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)E};
+  const uint32_t bw[3] = {64, 128, 1};
+  if (!make_map(&ma, A, 2, da, ba) || !make_map(&md, Wd, 3, dw, bw)) return MOE_ERR_CUDA;
+  Params p = base_params(off, N, E, status);
+  p.Kd = I;
+  p.I = I;
+  p.Nout = H;
+  p.n_tiles = (H + 255) / 256;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  return launch<kFwdDown>(ma, md, md, p, s);
+}
+
+int launch_mlp_grad_bf16(const void* dY, const void* X, const void* act, const void* gate_up,
+                         const int32_t* off, int N, int H, int I, int E, const void* Wg,
+                         const void* Wu, const void* Wd, void* dgu, void* dX, void* dWg,
+                         void* dWu, void* dWd, int32_t* status, cudaStream_t s) {
+  if (int rc = device_ok()) return rc;
+  const uint32_t box_k[2] = {64, 128};  // K-major row tiles
+  const uint32_t box_mn2[2] = {64, 64};  // MN-major 2-D boxes
+  const uint32_t box_mn3[3] = {64, 64, 1};
+  int rc;
+  if (N > 0) {
+    // 1. dA = dY Wd -> SwiGLU backward -> dgu
+    CUtensorMap m_dy, m_wd;
+    const uint64_t d_dy[2] = {(uint64_t)H, (uint64_t)N};
+    const uint64_t d_wd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)E};
+    if (!make_map(&m_dy, dY, 2, d_dy, box_k) || !make_map(&m_wd, Wd, 3, d_wd, box_mn3)) return MOE_ERR_CUDA;
+    Params p = base_params(off, N, E, status);
+    p.Kd = H;
+    p.I = I;
+    p.Nout = I;
+    p.n_tiles = (I + 255) / 256;
+    p.out = static_cast<__nv_bfloat16*>(dgu);
+    p.aux = static_cast<const __nv_bfloat16*>(gate_up);
+    if ((rc = launch<kDgradDown>(m_dy, m_wd, m_wd, p, s))) return rc;
+    // 2. dX = [dg | du] [Wg ; Wu]
+    CUtensorMap m_dgu, m_wg, m_wu;
+    const uint64_t d_dgu[2] = {(uint64_t)2 * I, (uint64_t)N};
+    const uint64_t d_w[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)E};
+    if (!make_map(&m_dgu, dgu, 2, d_dgu, box_k) || !make_map(&m_wg, Wg, 3, d_w, box_mn3) ||
+        !make_map(&m_wu, Wu, 3, d_w, box_mn3))
+      return MOE_ERR_CUDA;
+    Params q = base_params(off, N, E, status);
+    q.Kd = 2 * I;
+    q.I = I;
+    q.Nout = H;
+    q.n_tiles = (H + 255) / 256;
+    q.out = static_cast<__nv_bfloat16*>(dX);
+    if ((rc = launch<kDgradGateUp>(m_dgu, m_wg, m_wu, q, s))) return rc;
+  }
+  // 3. dWd[e] = dY_e^T act_e   (zeros for experts without rows)
+  {
+    CUtensorMap m_a, m_b;
+    const uint64_t d_a[2] = {(uint64_t)H, (uint64_t)(N > 0 ? N : 1)};
+    const uint64_t d_b[2] = {(uint64_t)I, (uint64_t)(N > 0 ? N : 1)};
+    if (!make_map(&m_a, N > 0 ? dY : dWd, 2, d_a, box_mn2) ||
+        !make_map(&m_b, N > 0 ? act : dWd, 2, d_b, box_mn2))
+      return MOE_ERR_CUDA;
+    Params p = base_params(off, N, E, status);
+    p.I = I;
+    p.Mout = H;
+    p.Nout = I;
+    p.m_tiles = (H + 127) / 128;
+    p.n_tiles = (I + 255) / 256;
+    p.out = static_cast<__nv_bfloat16*>(dWd);
+    if ((rc = launch<kWgradDown>(m_a, m_b, m_b, p, s))) return rc;
+  }
+  // 4. [dWg ; dWu][e] = dgu_e^T X_e
+  {
+    CUtensorMap m_a, m_b;
+    const uint64_t d_a[2] = {(uint64_t)2 * I, (uint64_t)(N > 0 ? N : 1)};
+    const uint64_t d_b[2] = {(uint64_t)H, (uint64_t)(N > 0 ? N : 1)};
+    if (!make_map(&m_a, N > 0 ? dgu : dWg, 2, d_a, box_mn2) ||
+        !make_map(&m_b, N > 0 ? X : dWg, 2, d_b, box_mn2))
+      return MOE_ERR_CUDA;
+    Params p = base_params(off, N, E, status);
+    p.I = I;
+    p.Mout = 2 * I;
+    p.Nout = H;
+    p.m_tiles = (2 * I + 127) / 128;
+    p.n_tiles = (H + 255) / 256;
+    p.out = static_cast<__nv_bfloat16*>(dWg);
+    p.out2 = static_cast<__nv_bfloat16*>(dWu);
+    if ((rc = launch<kWgradGateUp>(m_a, m_b, m_b, p, s))) return rc;
+  }
+  return MOE_OK;
 }
 
 }  // namespace moe

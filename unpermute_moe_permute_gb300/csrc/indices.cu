@@ -128,6 +128,7 @@ extern "C" int moe_permute_indices(const int32_t* counts, int R, int E, int32_t*
   grid = max(1, min(grid, sm_count()));
   permute_indices_kernel<<<grid, kIdxThreads, 0, stream>>>(counts, R, E, indices, capacity,
                                                            tokens_per_expert, total, dev_status);
+  count_launches(1);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -247,6 +247,7 @@ extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_
     // Nothing routed: zero counts, zero offsets.
     fill_kernel<<<1, 256, 0, stream>>>(tokens_per_expert, E, 0);
     fill_kernel<<<1, 256, 0, stream>>>(expert_offsets, E + 1, 0);
+    count_launches(2);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -261,11 +262,13 @@ extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_
                          (int)scatter_smem);
   route_scatter_kernel<<<nblk, kRouteThreads, scatter_smem, stream>>>(expert_ids, TK, K, E, E_total,
                                                                       blk, sorted_indices, row_map);
+  count_launches(3);
   if (tokens != nullptr && T > 0) {
     const int row_bytes = H * dtype_size(dtype);
     permute_rows_kernel<4><<<(T + 7) / 8, 256, 0, stream>>>(
         static_cast<const uint8_t*>(tokens), row_map, T, K, row_bytes,
         static_cast<uint8_t*>(permuted));
+    count_launches(1);
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -278,7 +281,10 @@ extern "C" int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, i
   if (!row_map || (N > 0 && !sorted_indices)) return MOE_ERR_INVALID_ARG;
   const int grid = min((TK + 255) / 256, 4 * sm_count());
   fill_kernel<<<grid, 256, 0, stream>>>(row_map, TK, -1);
-  if (N > 0) invert_kernel<<<min((N + 255) / 256, 4 * sm_count()), 256, 0, stream>>>(sorted_indices, N, TK, row_map);
+  if (N > 0)
+    invert_kernel<<<min((N + 255) / 256, 4 * sm_count()), 256, 0, stream>>>(sorted_indices, N, TK,
+                                                                             row_map);
+  count_launches(N > 0 ? 2 : 1);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -26,7 +26,7 @@ __device__ __forceinline__ ExpertRows expert_rows(const int32_t* __restrict__ of
 // prefix[e] = number of m-tiles of experts < e, prefix[E] = total.  Called by
 // every thread of the CTA (contains __syncthreads).  prefix: smem, E+1 ints;
 // scratch: smem, 32 ints.
-__device__ void build_tile_prefix(const int32_t* __restrict__ off, int E, int N, int BM,
+__device__ inline void build_tile_prefix(const int32_t* __restrict__ off, int E, int N, int BM,
                                   int32_t* prefix, int32_t* scratch) {
   const int nthr = blockDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
