@@ -14,8 +14,12 @@ input that is already resident in HBM (seeded generators of moe_inputs.py):
   permute_unpermute  T=16384 H=4096 E=64 K=8 bf16: permute -> unpermute ->
                      unpermute backward -> permute backward
 
-The default workload is layer_fwd_bwd when the bf16 expert-MLP kernels are
-available, else permute_unpermute.  The metric is tokens/s of the whole job
+The default workload is layer_fwd_bwd.  ``components`` adds the kernels of
+the other workloads, measured the same way after the timed region:
+permute_unpermute (permute/unpermute HBM GB/s), layer_forward (T=8192 H=2048
+E=256 K=8 I=512 with Zipf(1.2) routing: grouped GEMM TFLOP/s) and
+index_combine (index generation from counts[16 x 16] and the combine of
+T=4096 H=7168 K=8 with 12 special experts).  The metric is tokens/s of the whole job
 (all ranks).  Per-kernel CUDA-event times inside the timed region give each
 kernel's achieved HBM GB/s or TFLOP/s; the dominant kernel goes into the
 ``roofline`` object against the measured peaks in MEASURED_PEAKS.json.
@@ -284,26 +288,271 @@ class PermuteUnpermute:
         return out, gt, gprob
 
 
-WORKLOADS = {"permute_unpermute": PermuteUnpermute}
+def _gemm_bytes(T, H, E_active, E, K, I, bf=2):
+    """Algorithmic bytes and flops of each call of the bf16 layer (each
+    operand read once, each result written once; weights of experts that
+    have rows are read, weight grads of every expert are written)."""
+    N = T * K
+    idx = N * 4
+    w_gu, w_d = E_active * 2 * I * H * bf, E_active * H * I * bf
+    by = {
+        "permute": T * H * bf + N * H * bf + 4 * idx,
+        "gate_up_swiglu": N * H * bf + w_gu + N * I * bf + N * 2 * I * bf,
+        "gate_up_swiglu_nosave": N * H * bf + w_gu + N * I * bf,
+        "down_proj": N * I * bf + w_d + N * H * bf,
+        "unpermute": N * H * bf + T * H * bf + idx + N * 4,
+        "unpermute_grad": T * H * bf + 2 * N * H * bf + idx + 2 * N * 4,
+        "down_dgrad_swiglu": N * H * bf + w_d + 2 * N * 2 * I * bf,
+        "gate_up_dgrad": N * 2 * I * bf + w_gu + N * H * bf,
+        "down_wgrad": N * H * bf + N * I * bf + E * H * I * bf,
+        "gate_up_wgrad": N * 2 * I * bf + N * H * bf + E * 2 * I * H * bf,
+        "permute_grad": N * H * bf + T * H * bf + idx,
+    }
+    fl = {
+        "gate_up_swiglu": 2.0 * N * H * 2 * I,
+        "gate_up_swiglu_nosave": 2.0 * N * H * 2 * I,
+        "down_proj": 2.0 * N * I * H,
+        "down_dgrad_swiglu": 2.0 * N * H * I,
+        "gate_up_dgrad": 2.0 * N * 2 * I * H,
+        "down_wgrad": 2.0 * N * H * I,
+        "gate_up_wgrad": 2.0 * N * 2 * I * H,
+    }
+    return by, fl
+
+
+class LayerFwdBwd:
+    """T=4096 H=2048 E=128 K=8 I=768 bf16: forward and backward of the layer."""
+
+    name = "layer_fwd_bwd"
+    oracle_start_tokens = 256  # amortises the oracle's per-expert weight reads
+
+    @staticmethod
+    def available(lib):
+        return True
+
+    def __init__(self, lib, dev, seed=0, gen=moe_inputs.layer_fwd_bwd, backward=True, **kw):
+        d = gen(seed, **kw)
+        self.lib, self.dev, self.backward = lib, dev, backward
+        T, H, E, K, I = d["T"], d["H"], d["E"], d["K"], d["I"]
+        self.T, self.H, self.E, self.K, self.I = T, H, E, K, I
+        keys = ("tokens", "expert_ids", "probs") + (("grad_out",) if backward else ())
+        self.host = {k: d[k] for k in keys}
+        self.x = {k: v.to(dev) for k, v in self.host.items()}
+        self.Wg, self.Wu, self.Wd = d["W_gate"].to(dev), d["W_up"].to(dev), d["W_down"].to(dev)
+        N = T * K
+        bf = torch.bfloat16
+        e = lambda *shape, dt=bf: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+        self.permuted, self.sorted, self.row_map = e(N, H), e(N, dt=torch.int32), e(N, dt=torch.int32)
+        self.tpe, self.off = e(E, dt=torch.int32), e(E + 1, dt=torch.int32)
+        self.ws = e(max(lib.moe_permute_workspace_size(T, K, E), 16), dt=torch.uint8)
+        self.act, self.expanded, self.out = e(N, I), e(N, H), e(T, H)
+        self.gu = e(N, 2 * I) if backward else None
+        if backward:
+            self.gexp, self.gprobs, self.dgu, self.dperm = e(N, H), e(T, K, dt=torch.float32), e(N, 2 * I), e(N, H)
+            self.dWg, self.dWu, self.dWd = torch.empty_like(self.Wg), torch.empty_like(self.Wu), torch.empty_like(self.Wd)
+            self.gtok = e(T, H)
+        counts = np.bincount(d["expert_ids"].numpy().reshape(-1), minlength=E)
+        self.E_active = int((counts > 0).sum())
+        by, fl = _gemm_bytes(T, H, self.E_active, E, K, I)
+        if not backward:
+            by["gate_up_swiglu"], fl["gate_up_swiglu"] = by["gate_up_swiglu_nosave"], fl["gate_up_swiglu_nosave"]
+        self.bytes, self.flops = by, fl
+        self.config = {"workload": f"{'layer_fwd_bwd' if backward else 'layer_forward'}: "
+                                   f"T={T} H={H} E={E} K={K} I={I} bf16, fp32 probs",
+                       "T": T, "H": H, "E": E, "K": K, "I": I, "experts_with_rows": self.E_active,
+                       "l2": "inputs larger than L2 (weights alone exceed it), no flush"}
+
+    @classmethod
+    def host_only(cls, seed=0):
+        """The workload's host inputs only (no GPU): for the CPU oracle."""
+        w = cls.__new__(cls)
+        d = moe_inputs.layer_fwd_bwd(seed)
+        w.T, w.H, w.E, w.K, w.I, w.backward = d["T"], d["H"], d["E"], d["K"], d["I"], True
+        w.host = {k: d[k] for k in ("tokens", "expert_ids", "probs", "grad_out")}
+        w.Wg, w.Wu, w.Wd = d["W_gate"], d["W_up"], d["W_down"]
+        w.config = {"workload": f"layer_fwd_bwd: T={w.T} H={w.H} E={w.E} K={w.K} I={w.I} bf16, "
+                                "fp32 probs"}
+        return w
+
+    def step(self, t: Timers, x=None):
+        lib, x = self.lib, (x or self.x)
+        T, K, E = self.T, self.K, self.E
+        with t("permute"):
+            lib.moe_permute(x["tokens"], x["expert_ids"], E, 0, permuted=self.permuted,
+                            sorted_indices=self.sorted, row_map=self.row_map,
+                            tokens_per_expert=self.tpe, expert_offsets=self.off, workspace=self.ws)
+        with t("gate_up_swiglu"):
+            lib.moe_gate_up_swiglu(self.permuted, self.off, self.Wg, self.Wu, act=self.act,
+                                   gate_up_save=self.gu)
+        with t("down_proj"):
+            lib.moe_down_proj(self.act, self.off, self.Wd, expanded=self.expanded)
+        with t("unpermute"):
+            lib.moe_unpermute(self.expanded, self.row_map, x["probs"], T, K, out=self.out)
+        if not self.backward:
+            return
+        with t("unpermute_grad"):
+            lib.moe_unpermute_grad(x["grad_out"], self.expanded, self.row_map, x["probs"], K,
+                                   grad_permuted=self.gexp, grad_probs=self.gprobs)
+        with t("down_dgrad_swiglu"):
+            lib.moe_down_dgrad_swiglu(self.gexp, self.gu, self.off, self.Wd, dgu=self.dgu)
+        with t("gate_up_dgrad"):
+            lib.moe_gate_up_dgrad(self.dgu, self.off, self.Wg, self.Wu, d_permuted=self.dperm)
+        with t("down_wgrad"):
+            lib.moe_down_wgrad(self.gexp, self.act, self.off, dW_down=self.dWd)
+        with t("gate_up_wgrad"):
+            lib.moe_gate_up_wgrad(self.dgu, self.permuted, self.off, dW_gate=self.dWg, dW_up=self.dWu)
+        with t("permute_grad"):
+            lib.moe_permute_grad(self.dperm, self.row_map, T, K, out=self.gtok)
+
+    def results(self):
+        return [self.out, self.gtok, self.gprobs] if self.backward else [self.out]
+
+    units_per_step = property(lambda self: self.T)
+
+    def oracle_sample(self, O, n_tokens: int, cache={}):
+        """Oracle forward (and backward) of the first n_tokens tokens."""
+        key = id(self)
+        if key not in cache:  # bf16 -> float64 decode of the weights, done once
+            cache.clear()
+            cache[key] = tuple(w.float().cpu().numpy().astype(np.float64)
+                               for w in (self.Wg, self.Wu, self.Wd))
+        Wg, Wu, Wd = cache[key]
+        d = self.host
+        T, K, E = n_tokens, self.K, self.E
+        ids = d["expert_ids"][:T].numpy()
+        tok = d["tokens"][:T].float().numpy().astype(np.float64)
+        probs = d["probs"][:T].numpy()
+        si, rm, tpe, off = O.permute_routing(ids, E)
+        perm = O.permute_rows(tok, si, K)
+        act, y, _, _ = O.expert_mlp(perm, off, Wg, Wu, Wd, "bf16")
+        out = O.unpermute(y, rm, probs, T, K, "bf16")
+        if not self.backward:
+            return out
+        gout = d["grad_out"][:T].float().numpy().astype(np.float64)
+        gy, gp = O.unpermute_grad(gout, y, rm, probs, T, K, "bf16")
+        dperm, dWg, dWu, dWd = O.expert_mlp_grad(gy, perm, act, off, Wg, Wu, Wd, "bf16")
+        return out, O.permute_grad(dperm, rm, T, K, "bf16"), gp
+
+
+class LayerForward(LayerFwdBwd):
+    """T=8192 H=2048 E=256 K=8 I=512 bf16 forward, Zipf(1.2) routing."""
+
+    name = "layer_forward"
+
+    def __init__(self, lib, dev, seed=0, **kw):
+        super().__init__(lib, dev, seed, gen=moe_inputs.layer_forward_zipf, backward=False, **kw)
+
+
+class IndexCombine:
+    """Permute-index generation from counts[16 x 16] and the combine of
+    T=4096 H=7168 K=8 over 256 real + 4 zero + 4 copy + 4 const experts."""
+
+    name = "index_combine"
+
+    def __init__(self, lib, dev, seed=0):
+        d = moe_inputs.index_combine(seed)
+        self.lib = lib
+        self.d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in d.items()}
+        T, K, H = d["T"], d["K"], d["H"]
+        self.R, self.El = d["R"], d["E_local"]
+        self.total = int(d["counts"].sum())
+        self.idx = torch.empty(self.total, dtype=torch.int32, device=dev)
+        self.tpe = torch.empty(self.El, dtype=torch.int32, device=dev)
+        self.tot = torch.empty(1, dtype=torch.int32, device=dev)
+        nsp = d["zero_num"] + d["copy_num"] + d["const_num"]
+        self.routing = lib.moe_permute(None, self.d["expert_ids"], d["E"], nsp)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        n_real = d["expanded"].shape[0]
+        ids = d["expert_ids"].numpy()
+        n_ori = int(((ids >= d["E"] + d["zero_num"]).any(axis=1)).sum())
+        self.bytes = {"combine": n_real * H * 2 + n_ori * H * 2 + 2 * T * H * 2 + T * K * 12,
+                      "permute_indices": self.R * self.El * 4 * 2 + self.total * 4}
+        self.flops = {}
+
+    def step(self, t: Timers, x=None):
+        d, lib = self.d, self.lib
+        with t("permute_indices"):
+            lib.moe_permute_indices(d["counts"], self.R, self.El, self.total, indices=self.idx,
+                                    tokens_per_expert=self.tpe, total=self.tot)
+        with t("combine"):
+            lib.moe_combine(d["expanded"], self.routing.row_map, d["expert_ids"], d["scales"], d["E"],
+                            shared_x=d["shared_x"], ori_x=d["ori_x"], zero_num=d["zero_num"],
+                            copy_num=d["copy_num"], const_num=d["const_num"], alpha1=d["alpha1"],
+                            alpha2=d["alpha2"], const_v=d["const_v"], out=self.out)
+
+
+WORKLOADS = {"permute_unpermute": PermuteUnpermute, "layer_fwd_bwd": LayerFwdBwd,
+             "layer_forward": LayerForward}
 
 
 def pick_workload(lib, requested: str):
     if requested != "auto":
         return WORKLOADS[requested]
-    if "layer_fwd_bwd" in WORKLOADS and getattr(WORKLOADS["layer_fwd_bwd"], "available",
-                                                lambda lib: False)(lib):
-        return WORKLOADS["layer_fwd_bwd"]
-    return WORKLOADS["permute_unpermute"]
+    return WORKLOADS["layer_fwd_bwd"]
+
+
+def kernel_table(per, work, peaks):
+    """Per-call figures from CUDA-event times: GB/s and TFLOP/s of the
+    algorithmic bytes/flops, their fractions of the measured peaks, and the
+    bound (the larger of flops/peak and bytes/bandwidth)."""
+    total = max(sum(v["total_ms"] for v in per.values()), 1e-9)
+    out = {}
+    for name, s in per.items():
+        sec = s["avg_ms"] * 1e-3
+        e = {"launches": s["launches"], "avg_us": s["avg_ms"] * 1e3, "share": s["total_ms"] / total}
+        by, fl = work.bytes.get(name), work.flops.get(name)
+        if by:
+            e["gbs"] = by / sec / 1e9
+            e["hbm_frac"] = e["gbs"] / peaks["hbm_gbs"]
+        if fl:
+            e["tflops"] = fl / sec / 1e12
+            e["tensor_frac"] = e["tflops"] / peaks["bf16_tflops_sustained"]
+            t_tc = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+            t_hbm = (by or 0) / (peaks["hbm_gbs"] * 1e9)
+            e["bound"] = "tensor" if t_tc >= t_hbm else "hbm"
+            e["roofline_frac"] = max(t_tc, t_hbm) / sec
+        else:
+            e["bound"] = "hbm"
+            if by:
+                e["roofline_frac"] = e["hbm_frac"]
+        out[name] = e
+    return out
+
+
+def measure(work, steps, warmup, sync_barrier=False):
+    t = Timers()
+    for _ in range(warmup):
+        work.step(t)
+    torch.cuda.synchronize()
+    t.enabled = True
+    for _ in range(steps):
+        work.step(t)
+    torch.cuda.synchronize()
+    return t.summary()
+
+
+def run_components(lib, dev, peaks, steps=10, warmup=3):
+    """The other workloads' headline kernels, measured the same way."""
+    comps = {}
+    for cls in (PermuteUnpermute, LayerForward, IndexCombine):
+        w = cls(lib, dev)
+        per = measure(w, steps, warmup)
+        comps[w.name if hasattr(w, "name") else cls.__name__] = {
+            "config": getattr(w, "config", {}).get("workload", cls.__doc__.strip().splitlines()[0] if cls.__doc__ else ""),
+            "kernels": kernel_table(per, w, peaks)}
+        del w
+        torch.cuda.empty_cache()
+    return comps
 
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def time_oracle(work, budget_s: float = 12.0, start_tokens: int = 64, max_tokens: int = 2048):
+def time_oracle(work, budget_s: float = 12.0, start_tokens: int = None, max_tokens: int = 2048):
     """Time the oracle on growing samples until one sample takes a few
     seconds, then repeat that sample within the budget.  Returns
     (tokens/s, cores, sample description)."""
     from oracle import moe_oracle as O
-    n = start_tokens
+    n = start_tokens or getattr(work, "oracle_start_tokens", 64)
     t0 = time.perf_counter()
     work.oracle_sample(O, n)
     dt = time.perf_counter() - t0
@@ -361,30 +610,21 @@ def run_ours(args, world, rank, local):
 
     # per-kernel figures and the dominant kernel
     per = timers.summary()
-    kernels = {}
-    for name, s in per.items():
-        entry = {"launches": s["launches"], "avg_us": s["avg_ms"] * 1e3,
-                 "share": s["total_ms"] / max(sum(v["total_ms"] for v in per.values()), 1e-9)}
-        if name in work.flops:
-            entry["tflops"] = work.flops[name] / (s["avg_ms"] * 1e-3) / 1e12
-        if name in work.bytes:
-            entry["gbs"] = work.bytes[name] / (s["avg_ms"] * 1e-3) / 1e9
-        kernels[name] = entry
+    kernels = kernel_table(per, work, peaks)
     dom = max(per, key=lambda n: per[n]["total_ms"])
-    if dom in work.flops and work.flops[dom] / work.bytes.get(dom, 1) > 300:
-        achieved = kernels[dom]["tflops"]
-        peak = peaks["bf16_tflops_sustained"]
+    k = kernels[dom]
+    if k.get("bound") == "tensor":
+        achieved, peak = k["tflops"], peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
     else:
-        achieved = kernels[dom]["gbs"]
-        peak = peaks["hbm_gbs"]
+        achieved, peak = k["gbs"], peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
     roof["frac"] = achieved / peak
     roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    tr = recorded_traffic(dom)
-    roof["traffic"] = tr
+    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback")
+    roof["traffic"] = recorded_traffic(dom)
     roof["algorithmic_bytes"] = work.bytes.get(dom)
+    roof["algorithmic_flops"] = work.flops.get(dom)
 
     # end to end through the same calls with host buffers
     e2e = run_e2e(work, args, dev, world)
@@ -409,6 +649,8 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "e2e": e2e,
     }
+    if not args.no_components and world == 1:
+        result["components"] = run_components(lib, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = time_oracle(work)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
@@ -449,20 +691,16 @@ def run_e2e(work, args, dev, world):
 
 
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle timed on bounded samples."""
+    """The reference arm: the CPU oracle timed on bounded samples of the same
+    workload (one sample per step)."""
     if rank != 0:
         return
     from oracle import moe_oracle as O
-
-    class _Host:
-        pass
-
-    work = PermuteUnpermute.__new__(PermuteUnpermute)
-    d = moe_inputs.permute_unpermute(0)
-    work.T, work.H, work.E, work.K = d["T"], d["H"], d["E"], d["K"]
-    work.host = {k: d[k] for k in ("tokens", "expert_ids", "probs", "grad_out")}
-    n = 256
-    for _ in range(args.warmup):
+    work = LayerFwdBwd.host_only(0)
+    n = 8  # tokens per step: the oracle's cost is dominated by reading the expert weights
+    t0 = time.perf_counter()
+    work.oracle_sample(O, n)  # also decodes the weights once
+    for _ in range(max(0, args.warmup - 1)):
         work.oracle_sample(O, n)
     t0 = time.perf_counter()
     for _ in range(args.steps):
@@ -470,14 +708,14 @@ def run_reference(args, world, rank):
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
     cores = os.cpu_count() or 1
-    sample = f"{n}-token prefix of permute_unpermute_bwd per step, float64 numpy oracle"
+    sample = (f"first {n} tokens of the layer_fwd_bwd batch per step (forward + backward), "
+              "float64 numpy oracle")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded moe_inputs generators)",
-        "config": {"workload": "permute_unpermute_bwd: T=16384 H=4096 E=64 K=8 (oracle sample)",
-                   "parallelism": "cpu"},
+        "config": dict(work.config, parallelism="cpu"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -493,6 +731,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-components", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

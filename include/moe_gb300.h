@@ -235,6 +235,26 @@ int moe_expert_mlp_grad(const void* grad_expanded, const void* permuted, const v
                         const void* W_down, void* dgu, void* d_permuted, void* dW_gate,
                         void* dW_up, void* dW_down, int32_t* dev_status, cudaStream_t stream);
 
+/* The four grouped GEMMs of moe_expert_mlp_grad, one kernel each, in the
+ * order that call runs them (bf16 only).  A caller whose expert weights are
+ * frozen (adapter training) runs the two dgrads and skips the wgrads.
+ *   moe_down_dgrad_swiglu: dgu = SwiGLU-backward(grad_expanded W_down[e], g, u)
+ *   moe_gate_up_dgrad:     d_permuted = dg W_gate[e] + du W_up[e]
+ *   moe_down_wgrad:        dW_down[e] = grad_expanded_e^T act_e
+ *   moe_gate_up_wgrad:     dW_gate[e] = dg_e^T X_e,  dW_up[e] = du_e^T X_e  */
+int moe_down_dgrad_swiglu(const void* grad_expanded, const void* gate_up_save, int dtype,
+                          const int32_t* expert_offsets, int N, int H, int I, int E,
+                          const void* W_down, void* dgu, int32_t* dev_status, cudaStream_t stream);
+int moe_gate_up_dgrad(const void* dgu, int dtype, const int32_t* expert_offsets, int N, int H,
+                      int I, int E, const void* W_gate, const void* W_up, void* d_permuted,
+                      int32_t* dev_status, cudaStream_t stream);
+int moe_down_wgrad(const void* grad_expanded, const void* act, int dtype,
+                   const int32_t* expert_offsets, int N, int H, int I, int E, void* dW_down,
+                   int32_t* dev_status, cudaStream_t stream);
+int moe_gate_up_wgrad(const void* dgu, const void* permuted, int dtype,
+                      const int32_t* expert_offsets, int N, int H, int I, int E, void* dW_gate,
+                      void* dW_up, int32_t* dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

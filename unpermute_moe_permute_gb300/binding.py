@@ -67,6 +67,10 @@ _SIGNATURES = {
     "moe_permute_indices": ([_P, _I, _I, _P, _I, _P, _P, _P, _P], _I),
     "moe_expert_mlp_grad": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                              _P, _P, _P, _P], _I),
+    "moe_down_dgrad_swiglu": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_gate_up_dgrad": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_down_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_gate_up_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
 }
 
 
@@ -262,6 +266,43 @@ def moe_expert_mlp_grad(grad_expanded, permuted, act, gate_up_save, expert_offse
           _ptr(W_up), _ptr(W_down), _ptr(dgu), _ptr(d_permuted), _ptr(dW_gate), _ptr(dW_up),
           _ptr(dW_down), _ptr(dev_status), _stream())
     return d_permuted, dW_gate, dW_up, dW_down
+
+
+def moe_down_dgrad_swiglu(grad_expanded, gate_up_save, expert_offsets, W_down, *, dgu=None,
+                          dev_status=None):
+    N, H = grad_expanded.shape
+    E, _, I = W_down.shape
+    if dgu is None:
+        dgu = torch.empty((N, 2 * I), dtype=grad_expanded.dtype, device=grad_expanded.device)
+    _call("moe_down_dgrad_swiglu", _ptr(grad_expanded), _ptr(gate_up_save), _dtype(grad_expanded),
+          _ptr(expert_offsets), N, H, I, E, _ptr(W_down), _ptr(dgu), _ptr(dev_status), _stream())
+    return dgu
+
+
+def moe_gate_up_dgrad(dgu, expert_offsets, W_gate, W_up, *, d_permuted=None, dev_status=None):
+    N = dgu.shape[0]
+    E, I, H = W_gate.shape
+    if d_permuted is None:
+        d_permuted = torch.empty((N, H), dtype=dgu.dtype, device=dgu.device)
+    _call("moe_gate_up_dgrad", _ptr(dgu), _dtype(dgu), _ptr(expert_offsets), N, H, I, E,
+          _ptr(W_gate), _ptr(W_up), _ptr(d_permuted), _ptr(dev_status), _stream())
+    return d_permuted
+
+
+def moe_down_wgrad(grad_expanded, act, expert_offsets, *, dW_down, dev_status=None):
+    N, H = grad_expanded.shape
+    E, _, I = dW_down.shape
+    _call("moe_down_wgrad", _ptr(grad_expanded), _ptr(act), _dtype(grad_expanded),
+          _ptr(expert_offsets), N, H, I, E, _ptr(dW_down), _ptr(dev_status), _stream())
+    return dW_down
+
+
+def moe_gate_up_wgrad(dgu, permuted, expert_offsets, *, dW_gate, dW_up, dev_status=None):
+    N, H = permuted.shape
+    E, I, _ = dW_gate.shape
+    _call("moe_gate_up_wgrad", _ptr(dgu), _ptr(permuted), _dtype(permuted), _ptr(expert_offsets),
+          N, H, I, E, _ptr(dW_gate), _ptr(dW_up), _ptr(dev_status), _stream())
+    return dW_gate, dW_up
 
 
 # ---------------------------------------------------------------- unpermute / combine

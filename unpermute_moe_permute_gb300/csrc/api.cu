@@ -1,6 +1,7 @@
 // C-ABI glue: status strings, device status readback, argument checks and
 // dtype dispatch of the expert-MLP GEMMs.
 #include <atomic>
+#include <initializer_list>
 
 #include "common.cuh"
 
@@ -14,10 +15,17 @@ int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const
                             cudaStream_t s);
 int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int N, int H, int I,
                          int E, void* out, int32_t* status, cudaStream_t s);
-int launch_mlp_grad_bf16(const void* dY, const void* X, const void* act, const void* gate_up,
-                         const int32_t* off, int N, int H, int I, int E, const void* Wg,
-                         const void* Wu, const void* Wd, void* dgu, void* dX, void* dWg,
-                         void* dWu, void* dWd, int32_t* status, cudaStream_t s);
+int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* off, int N, int H,
+                           int I, int E, const void* Wd, void* dgu, int32_t* status,
+                           cudaStream_t s);
+int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H, int I, int E,
+                              const void* Wg, const void* Wu, void* dX, int32_t* status,
+                              cudaStream_t s);
+int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, int N, int H,
+                           int I, int E, void* dWd, int32_t* status, cudaStream_t s);
+int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
+                              int I, int E, void* dWg, void* dWu, int32_t* status,
+                              cudaStream_t s);
 
 static std::atomic<unsigned long long> g_launches{0};
 
@@ -137,23 +145,77 @@ extern "C" int moe_expert_mlp(const void* permuted, int dtype, const int32_t* ex
                        stream);
 }
 
+static int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+extern "C" int moe_down_dgrad_swiglu(const void* grad_expanded, const void* gate_up_save,
+                                     int dtype, const int32_t* expert_offsets, int N, int H,
+                                     int I, int E, const void* W_down, void* dgu,
+                                     int32_t* dev_status, cudaStream_t stream) {
+  if (int rc = check_mlp(grad_expanded, dtype, expert_offsets, N, H, I, E)) return rc;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (N == 0) return MOE_OK;
+  if (int rc = check_ptrs({grad_expanded, gate_up_save, W_down, dgu})) return rc;
+  return launch_down_dgrad_bf16(grad_expanded, gate_up_save, expert_offsets, N, H, I, E, W_down,
+                                dgu, dev_status, stream);
+}
+
+extern "C" int moe_gate_up_dgrad(const void* dgu, int dtype, const int32_t* expert_offsets, int N,
+                                 int H, int I, int E, const void* W_gate, const void* W_up,
+                                 void* d_permuted, int32_t* dev_status, cudaStream_t stream) {
+  if (int rc = check_mlp(dgu, dtype, expert_offsets, N, H, I, E)) return rc;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (N == 0) return MOE_OK;
+  if (int rc = check_ptrs({dgu, W_gate, W_up, d_permuted})) return rc;
+  return launch_gate_up_dgrad_bf16(dgu, expert_offsets, N, H, I, E, W_gate, W_up, d_permuted,
+                                   dev_status, stream);
+}
+
+extern "C" int moe_down_wgrad(const void* grad_expanded, const void* act, int dtype,
+                              const int32_t* expert_offsets, int N, int H, int I, int E,
+                              void* dW_down, int32_t* dev_status, cudaStream_t stream) {
+  if (int rc = check_mlp(grad_expanded, dtype, expert_offsets, N, H, I, E)) return rc;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (int rc = check_ptrs({dW_down})) return rc;
+  if (N > 0)
+    if (int rc = check_ptrs({grad_expanded, act})) return rc;
+  return launch_down_wgrad_bf16(grad_expanded, act, expert_offsets, N, H, I, E, dW_down,
+                                dev_status, stream);
+}
+
+extern "C" int moe_gate_up_wgrad(const void* dgu, const void* permuted, int dtype,
+                                 const int32_t* expert_offsets, int N, int H, int I, int E,
+                                 void* dW_gate, void* dW_up, int32_t* dev_status,
+                                 cudaStream_t stream) {
+  if (int rc = check_mlp(dgu, dtype, expert_offsets, N, H, I, E)) return rc;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (int rc = check_ptrs({dW_gate, dW_up})) return rc;
+  if (N > 0)
+    if (int rc = check_ptrs({dgu, permuted})) return rc;
+  return launch_gate_up_wgrad_bf16(dgu, permuted, expert_offsets, N, H, I, E, dW_gate, dW_up,
+                                   dev_status, stream);
+}
+
 extern "C" int moe_expert_mlp_grad(const void* grad_expanded, const void* permuted,
                                    const void* act, const void* gate_up_save, int dtype,
                                    const int32_t* expert_offsets, int N, int H, int I, int E,
                                    const void* W_gate, const void* W_up, const void* W_down,
                                    void* dgu, void* d_permuted, void* dW_gate, void* dW_up,
                                    void* dW_down, int32_t* dev_status, cudaStream_t stream) {
-  int rc = check_mlp(grad_expanded, dtype, expert_offsets, N, H, I, E);
+  int rc = moe_down_dgrad_swiglu(grad_expanded, gate_up_save, dtype, expert_offsets, N, H, I, E,
+                                 W_down, dgu, dev_status, stream);
   if (rc) return rc;
-  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  if (!W_gate || !W_up || !W_down || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
-  if (N > 0 && (!permuted || !act || !gate_up_save || !dgu || !d_permuted))
-    return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {grad_expanded, permuted, act,     gate_up_save, W_gate, W_up,
-                        W_down,        dgu,      d_permuted, dW_gate,    dW_up,  dW_down};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
-  return launch_mlp_grad_bf16(grad_expanded, permuted, act, gate_up_save, expert_offsets, N, H, I,
-                              E, W_gate, W_up, W_down, dgu, d_permuted, dW_gate, dW_up, dW_down,
-                              dev_status, stream);
+  rc = moe_gate_up_dgrad(dgu, dtype, expert_offsets, N, H, I, E, W_gate, W_up, d_permuted,
+                         dev_status, stream);
+  if (rc) return rc;
+  rc = moe_down_wgrad(grad_expanded, act, dtype, expert_offsets, N, H, I, E, dW_down, dev_status,
+                      stream);
+  if (rc) return rc;
+  return moe_gate_up_wgrad(dgu, permuted, dtype, expert_offsets, N, H, I, E, dW_gate, dW_up,
+                           dev_status, stream);
 }

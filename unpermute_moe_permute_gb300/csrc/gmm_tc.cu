@@ -572,80 +572,94 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   return launch<kFwdDown>(ma, md, md, p, s);
 }
 
-int launch_mlp_grad_bf16(const void* dY, const void* X, const void* act, const void* gate_up,
-                         const int32_t* off, int N, int H, int I, int E, const void* Wg,
-                         const void* Wu, const void* Wd, void* dgu, void* dX, void* dWg,
-                         void* dWu, void* dWd, int32_t* status, cudaStream_t s) {
+int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* off, int N, int H,
+                           int I, int E, const void* Wd, void* dgu, int32_t* status,
+                           cudaStream_t s) {
   if (int rc = device_ok()) return rc;
-  const uint32_t box_k[2] = {64, 128};  // K-major row tiles
-  const uint32_t box_mn2[2] = {64, 64};  // MN-major 2-D boxes
+  if (N == 0) return MOE_OK;
+  const uint32_t box_k[2] = {64, 128};
   const uint32_t box_mn3[3] = {64, 64, 1};
-  int rc;
-  if (N > 0) {
-    // 1. dA = dY Wd -> SwiGLU backward -> dgu
-    CUtensorMap m_dy, m_wd;
-    const uint64_t d_dy[2] = {(uint64_t)H, (uint64_t)N};
-    const uint64_t d_wd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)E};
-    if (!make_map(&m_dy, dY, 2, d_dy, box_k) || !make_map(&m_wd, Wd, 3, d_wd, box_mn3)) return MOE_ERR_CUDA;
-    Params p = base_params(off, N, E, status);
-    p.Kd = H;
-    p.I = I;
-    p.Nout = I;
-    p.n_tiles = (I + 255) / 256;
-    p.out = static_cast<__nv_bfloat16*>(dgu);
-    p.aux = static_cast<const __nv_bfloat16*>(gate_up);
-    if ((rc = launch<kDgradDown>(m_dy, m_wd, m_wd, p, s))) return rc;
-    // 2. dX = [dg | du] [Wg ; Wu]
-    CUtensorMap m_dgu, m_wg, m_wu;
-    const uint64_t d_dgu[2] = {(uint64_t)2 * I, (uint64_t)N};
-    const uint64_t d_w[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)E};
-    if (!make_map(&m_dgu, dgu, 2, d_dgu, box_k) || !make_map(&m_wg, Wg, 3, d_w, box_mn3) ||
-        !make_map(&m_wu, Wu, 3, d_w, box_mn3))
-      return MOE_ERR_CUDA;
-    Params q = base_params(off, N, E, status);
-    q.Kd = 2 * I;
-    q.I = I;
-    q.Nout = H;
-    q.n_tiles = (H + 255) / 256;
-    q.out = static_cast<__nv_bfloat16*>(dX);
-    if ((rc = launch<kDgradGateUp>(m_dgu, m_wg, m_wu, q, s))) return rc;
-  }
-  // 3. dWd[e] = dY_e^T act_e   (zeros for experts without rows)
-  {
-    CUtensorMap m_a, m_b;
-    const uint64_t d_a[2] = {(uint64_t)H, (uint64_t)(N > 0 ? N : 1)};
-    const uint64_t d_b[2] = {(uint64_t)I, (uint64_t)(N > 0 ? N : 1)};
-    if (!make_map(&m_a, N > 0 ? dY : dWd, 2, d_a, box_mn2) ||
-        !make_map(&m_b, N > 0 ? act : dWd, 2, d_b, box_mn2))
-      return MOE_ERR_CUDA;
-    Params p = base_params(off, N, E, status);
-    p.I = I;
-    p.Mout = H;
-    p.Nout = I;
-    p.m_tiles = (H + 127) / 128;
-    p.n_tiles = (I + 255) / 256;
-    p.out = static_cast<__nv_bfloat16*>(dWd);
-    if ((rc = launch<kWgradDown>(m_a, m_b, m_b, p, s))) return rc;
-  }
-  // 4. [dWg ; dWu][e] = dgu_e^T X_e
-  {
-    CUtensorMap m_a, m_b;
-    const uint64_t d_a[2] = {(uint64_t)2 * I, (uint64_t)(N > 0 ? N : 1)};
-    const uint64_t d_b[2] = {(uint64_t)H, (uint64_t)(N > 0 ? N : 1)};
-    if (!make_map(&m_a, N > 0 ? dgu : dWg, 2, d_a, box_mn2) ||
-        !make_map(&m_b, N > 0 ? X : dWg, 2, d_b, box_mn2))
-      return MOE_ERR_CUDA;
-    Params p = base_params(off, N, E, status);
-    p.I = I;
-    p.Mout = 2 * I;
-    p.Nout = H;
-    p.m_tiles = (2 * I + 127) / 128;
-    p.n_tiles = (H + 255) / 256;
-    p.out = static_cast<__nv_bfloat16*>(dWg);
-    p.out2 = static_cast<__nv_bfloat16*>(dWu);
-    if ((rc = launch<kWgradGateUp>(m_a, m_b, m_b, p, s))) return rc;
-  }
-  return MOE_OK;
+  CUtensorMap m_dy, m_wd;
+  const uint64_t d_dy[2] = {(uint64_t)H, (uint64_t)N};
+  const uint64_t d_wd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)E};
+  if (!make_map(&m_dy, dY, 2, d_dy, box_k) || !make_map(&m_wd, Wd, 3, d_wd, box_mn3))
+    return MOE_ERR_CUDA;
+  Params p = base_params(off, N, E, status);
+  p.Kd = H;
+  p.I = I;
+  p.Nout = I;
+  p.n_tiles = (I + 255) / 256;
+  p.out = static_cast<__nv_bfloat16*>(dgu);
+  p.aux = static_cast<const __nv_bfloat16*>(gate_up);
+  return launch<kDgradDown>(m_dy, m_wd, m_wd, p, s);
+}
+
+int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H, int I, int E,
+                              const void* Wg, const void* Wu, void* dX, int32_t* status,
+                              cudaStream_t s) {
+  if (int rc = device_ok()) return rc;
+  if (N == 0) return MOE_OK;
+  const uint32_t box_k[2] = {64, 128};
+  const uint32_t box_mn3[3] = {64, 64, 1};
+  CUtensorMap m_dgu, m_wg, m_wu;
+  const uint64_t d_dgu[2] = {(uint64_t)2 * I, (uint64_t)N};
+  const uint64_t d_w[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)E};
+  if (!make_map(&m_dgu, dgu, 2, d_dgu, box_k) || !make_map(&m_wg, Wg, 3, d_w, box_mn3) ||
+      !make_map(&m_wu, Wu, 3, d_w, box_mn3))
+    return MOE_ERR_CUDA;
+  Params q = base_params(off, N, E, status);
+  q.Kd = 2 * I;
+  q.I = I;
+  q.Nout = H;
+  q.n_tiles = (H + 255) / 256;
+  q.out = static_cast<__nv_bfloat16*>(dX);
+  return launch<kDgradGateUp>(m_dgu, m_wg, m_wu, q, s);
+}
+
+// With no rows at all the operand maps are never read (every tile has zero
+// k blocks); they point at the output so that they are well formed.
+int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, int N, int H,
+                           int I, int E, void* dWd, int32_t* status, cudaStream_t s) {
+  if (int rc = device_ok()) return rc;
+  const uint32_t box_mn2[2] = {64, 64};
+  CUtensorMap m_a, m_b;
+  const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
+  const uint64_t d_a[2] = {(uint64_t)H, rows};
+  const uint64_t d_b[2] = {(uint64_t)I, rows};
+  if (!make_map(&m_a, N > 0 ? dY : dWd, 2, d_a, box_mn2) ||
+      !make_map(&m_b, N > 0 ? act : dWd, 2, d_b, box_mn2))
+    return MOE_ERR_CUDA;
+  Params p = base_params(off, N, E, status);
+  p.I = I;
+  p.Mout = H;
+  p.Nout = I;
+  p.m_tiles = (H + 127) / 128;
+  p.n_tiles = (I + 255) / 256;
+  p.out = static_cast<__nv_bfloat16*>(dWd);
+  return launch<kWgradDown>(m_a, m_b, m_b, p, s);
+}
+
+int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
+                              int I, int E, void* dWg, void* dWu, int32_t* status,
+                              cudaStream_t s) {
+  if (int rc = device_ok()) return rc;
+  const uint32_t box_mn2[2] = {64, 64};
+  CUtensorMap m_a, m_b;
+  const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
+  const uint64_t d_a[2] = {(uint64_t)2 * I, rows};
+  const uint64_t d_b[2] = {(uint64_t)H, rows};
+  if (!make_map(&m_a, N > 0 ? dgu : dWg, 2, d_a, box_mn2) ||
+      !make_map(&m_b, N > 0 ? X : dWg, 2, d_b, box_mn2))
+    return MOE_ERR_CUDA;
+  Params p = base_params(off, N, E, status);
+  p.I = I;
+  p.Mout = 2 * I;
+  p.Nout = H;
+  p.m_tiles = (2 * I + 127) / 128;
+  p.n_tiles = (H + 255) / 256;
+  p.out = static_cast<__nv_bfloat16*>(dWg);
+  p.out2 = static_cast<__nv_bfloat16*>(dWu);
+  return launch<kWgradGateUp>(m_a, m_b, m_b, p, s);
 }
 
 }  // namespace moe
