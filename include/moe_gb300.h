@@ -124,6 +124,35 @@ int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T,
                 int32_t* tokens_per_expert, int32_t* expert_offsets, void* workspace,
                 size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
+/* moe_permute without a caller-provided workspace.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory themselves: a plugin that its host framework hands
+ * only input and output buffers, or a process whose device memory is all
+ * reserved by another allocator (a cudaMalloc there would fail, or
+ * synchronise the device at a bad moment).
+ *
+ * The per-block expert counts live in one file-scope device array of
+ * MOE_PERMUTE_STATIC_SCRATCH_INTS int32 (256 KiB) that every GPU which loads
+ * this library holds until the process exits.  It is enough when
+ * ceil(T*K / 2048) * E <= MOE_PERMUTE_STATIC_SCRATCH_INTS; larger problems
+ * return MOE_ERR_CAPACITY before anything is launched.
+ *   - The first call on a device looks up that device's address of the
+ *     array (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - Every call uses the same array, so calls whose kernels can overlap on
+ *     the GPU (different streams, no ordering between them) race with each
+ *     other and must be serialised by the caller.  The array keeps the last
+ *     call's contents; every entry a call reads is written by that call
+ *     first, so nothing needs clearing between calls.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Arguments and results are those of moe_permute. */
+#define MOE_PERMUTE_STATIC_SCRATCH_INTS 65536
+int moe_permute_static_scratch(const void* tokens, int dtype, const int32_t* expert_ids, int T,
+                               int H, int K, int E, int num_special, void* permuted,
+                               int32_t* sorted_indices, int32_t* row_map,
+                               int32_t* tokens_per_expert, int32_t* expert_offsets,
+                               int32_t* dev_status, cudaStream_t stream);
+
 /* Rebuild row_map [TK] from sorted_indices [N] (row_map[sorted[i]] = i,
  * every other entry -1).  For callers that keep only sorted_indices. */
 int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, int TK, int32_t* row_map,

@@ -56,6 +56,8 @@ _SIGNATURES = {
     "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
     "moe_permute": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "moe_invert_sorted_indices": ([_P, _I, _I, _P, _P], _I),
+    "moe_permute_static_scratch": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P],
+                                   _I),
     "moe_gate_up_swiglu": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_down_proj": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_expert_mlp": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
@@ -193,6 +195,40 @@ def moe_permute(tokens: Optional[torch.Tensor], expert_ids: torch.Tensor, num_ex
           num_special, _ptr(permuted), _ptr(sorted_indices), _ptr(row_map),
           _ptr(tokens_per_expert), _ptr(expert_offsets), _ptr(workspace),
           workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream())
+    return PermuteResult(permuted, sorted_indices, row_map, tokens_per_expert, expert_offsets)
+
+
+MOE_PERMUTE_STATIC_SCRATCH_INTS = 65536
+
+
+def moe_permute_static_scratch(tokens: Optional[torch.Tensor], expert_ids: torch.Tensor,
+                               num_experts: int, num_special: int = 0, *, permuted=None,
+                               sorted_indices=None, row_map=None, tokens_per_expert=None,
+                               expert_offsets=None, dev_status=None) -> PermuteResult:
+    """moe_permute for callers that cannot allocate device memory: the
+    library keeps the per-block counts in its own fixed device array
+    (MOE_PERMUTE_STATIC_SCRATCH_INTS int32), shared by every call, so calls
+    must not overlap on the GPU.  Outputs the caller does not pass are
+    allocated here by torch only for convenience of this binding."""
+    _check(expert_ids, torch.int32, "expert_ids")
+    T, K = expert_ids.shape
+    dev = expert_ids.device
+    H = tokens.shape[1] if tokens is not None else 0
+    dt = _dtype(tokens) if tokens is not None else MOE_BF16
+    TK = T * K
+    if tokens is not None and permuted is None:
+        permuted = torch.empty((TK, H), dtype=tokens.dtype, device=dev)
+    if sorted_indices is None:
+        sorted_indices = torch.empty(TK, dtype=torch.int32, device=dev)
+    if row_map is None:
+        row_map = torch.empty(TK, dtype=torch.int32, device=dev)
+    if tokens_per_expert is None:
+        tokens_per_expert = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    if expert_offsets is None:
+        expert_offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    _call("moe_permute_static_scratch", _ptr(tokens), dt, _ptr(expert_ids), T, max(H, 1), K,
+          num_experts, num_special, _ptr(permuted), _ptr(sorted_indices), _ptr(row_map),
+          _ptr(tokens_per_expert), _ptr(expert_offsets), _ptr(dev_status), _stream())
     return PermuteResult(permuted, sorted_indices, row_map, tokens_per_expert, expert_offsets)
 
 

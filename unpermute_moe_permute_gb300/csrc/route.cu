@@ -12,6 +12,8 @@
 // its K destinations with 16-byte vectors.  The rank pass is deterministic:
 // per-block counts -> per-(block, expert) bases -> per-warp bases -> in-warp
 // rank from __match_any_sync peers, so no atomic ordering reaches the output.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -287,4 +289,53 @@ extern "C" int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, i
   count_launches(N > 0 ? 2 : 1);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+// ---- allocation-free variant -------------------------------------------------
+//
+// Scratch for the per-block expert counts of moe_permute_static_scratch: one
+// array per device, alive for the whole process.  Host code must not pass
+// the symbol itself to a kernel (on the host it names a host-side shadow,
+// not device memory); the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) int32_t g_permute_scratch[MOE_PERMUTE_STATIC_SCRATCH_INTS];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_permute_scratch on the current device, looked up once
+// per device (with that device current).  nullptr on failure.
+int32_t* permute_scratch_address() {
+  static std::mutex mu;
+  static int32_t* addr[kMaxDevices] = {nullptr};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int moe_permute_static_scratch(const void* tokens, int dtype, const int32_t* expert_ids,
+                                          int T, int H, int K, int E, int num_special,
+                                          void* permuted, int32_t* sorted_indices,
+                                          int32_t* row_map, int32_t* tokens_per_expert,
+                                          int32_t* expert_offsets, int32_t* dev_status,
+                                          cudaStream_t stream) {
+  if (T < 0 || K <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_permute_workspace_size(T, K, E);
+  const size_t have = sizeof(int32_t) * MOE_PERMUTE_STATIC_SCRATCH_INTS;
+  if (need > have) return MOE_ERR_CAPACITY;
+  int32_t* scratch = permute_scratch_address();
+  if (scratch == nullptr) return MOE_ERR_CUDA;
+  return moe_permute(tokens, dtype, expert_ids, T, H, K, E, num_special, permuted, sorted_indices,
+                     row_map, tokens_per_expert, expert_offsets, scratch, have, dev_status, stream);
 }
