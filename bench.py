@@ -97,9 +97,10 @@ def barrier():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+    """nvidia-smi clock/throttle samples every 50 ms; the samples whose
+    timestamps fall inside the timed region are kept."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -115,12 +116,12 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin=None, t_end=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -134,14 +135,21 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                except (ValueError, IndexError):
+                    ts = None
+                if t_begin is not None and ts is not None and not (t_begin - 0.05 <= ts <= t_end + 0.05):
+                    continue
+                try:
+                    sm.append(float(parts[2]))
+                    smax.append(float(parts[3]))
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[5:9]):
+                for name, val in zip(names, parts[6:10]):
                     if val.lower().startswith("active"):
                         reasons.add(name)
         os.unlink(self.path)
@@ -582,26 +590,29 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = load_peaks()
     timers = Timers()
 
+    clocks = ClockSampler(local)
+    clocks.start()  # started before the warm-up so that it samples the whole timed region
     for _ in range(args.warmup):
         work.step(timers)
     torch.cuda.synchronize()
+    time.sleep(0.2)
     barrier()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    clocks.start()
     timers.enabled = True
     launches0 = lib.moe_kernel_launches()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
     start.record()
     for _ in range(args.steps):
         work.step(timers)
     end.record()
     torch.cuda.synchronize()
+    t_end = time.time()
     launches = lib.moe_kernel_launches() - launches0
     timers.enabled = False
-    clk = clocks.stop()
+    clk = clocks.stop(t_begin, t_end)
     barrier()
     elapsed_ms = start.elapsed_time(end)
     max_ms = reduce_max(elapsed_ms, dev)
@@ -726,7 +737,7 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="auto")

@@ -44,8 +44,15 @@ constexpr uint32_t B_BYTES = BN * BK * 2;        // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;   // one 64 (M/N) x 64 (K) box, 8 KB
 constexpr uint32_t TMEM_COLS = 512;
+// Epilogue staging: each epilogue warp owns a ring of NBUF units of 32 rows x
+// 32 bf16 (2 KB, 64-byte swizzle) that TMA stores copy to global memory.
+constexpr int NBUF = 2;
+constexpr uint32_t UNIT_BYTES = 32 * 64;
+constexpr uint32_t STAGING_BYTES = 4 * NBUF * UNIT_BYTES;  // 16 KB
 constexpr uint32_t CTRL_BYTES = 128 + (kMaxExperts + 1) * 4 + 32 * 4;
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + CTRL_BYTES + 1024;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + CTRL_BYTES + 1024;
+static_assert(8 * (2 * STAGES + 5) <= 104, "barriers overlap the control words");
+static_assert(SMEM_BYTES <= 232448, "more shared memory than one CTA may use");
 
 enum Kind : int {
   kFwdGateUp = 0,
@@ -158,22 +165,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Store 32 fp32 values (bit patterns) as 32 bf16 = 64 contiguous bytes.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
-  uint32_t pk[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) d[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-}
-
-__device__ __forceinline__ void store_zero32(__nv_bfloat16* dst) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) d[q] = make_uint4(0u, 0u, 0u, 0u);
-}
-
 __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&f)[32]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -190,97 +181,207 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&f)[
   }
 }
 
-// Epilogue of one tile for one thread: TMEM lane = output row of the tile.
+// ---- epilogue ---------------------------------------------------------------
+//
+// Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter).  It
+// converts 32-column pieces to bf16 into its staging ring (lane i writes row
+// i, 64-byte swizzle, so the warp's 16-byte stores hit distinct banks) and
+// one lane hands each 32 x 32 unit to a TMA store, which writes whole 64-byte
+// row segments.  Units that would cross the end of an expert's rows (the next
+// expert's rows follow) are copied out by the lanes whose rows are valid
+// instead.  Every unit commits one bulk group (an empty one for the copied
+// units), so the two-unit ring is recycled by counting groups.
+
+struct Ring {
+  uint32_t base;  // this warp's NBUF units
+  int slot;       // next unit to fill
+  // Next unit, once the store that last used it has read it.
+  __device__ __forceinline__ uint32_t next(int lane) {
+    if (lane == 0) bulk_wait_group_read<NBUF - 1>();
+    __syncwarp();
+    const uint32_t b = base + (uint32_t)(slot % NBUF) * UNIT_BYTES;
+    ++slot;
+    return b;
+  }
+};
+
+__device__ __forceinline__ void pack32(const uint32_t (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+}
+
+// 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint32_t unit_chunk(uint32_t buf, int r, int c) {
+  return buf + (uint32_t)r * 64u + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4);
+}
+
+__device__ __forceinline__ void stage_row(uint32_t buf, int lane, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4(unit_chunk(buf, lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+// Hand a staged unit to TMA (all 32 rows valid) or copy this lane's row to
+// `row_dst` (nullptr: row not written); then close the unit's bulk group.
+template <bool k3D>
+__device__ __forceinline__ void flush_unit(uint32_t buf, int lane, bool tma, const CUtensorMap* map,
+                                           int x, int y, int z, __nv_bfloat16* row_dst) {
+  if (tma) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (k3D) tma_store_3d(map, buf, x, y, z);
+      else tma_store_2d(map, buf, x, y);
+    }
+  } else {
+    if (row_dst != nullptr) {
+      uint4* d = reinterpret_cast<uint4*>(row_dst);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(unit_chunk(buf, lane, j)));
+        d[j] = v;
+      }
+    }
+    __syncwarp();
+  }
+  if (lane == 0) bulk_commit_group();
+}
+
+// Epilogue of one tile for one epilogue warp.  tacc: TMEM address of the
+// warp's lane quarter of the accumulator; quarter: which 32 rows.
 template <int KIND>
-__device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_t tacc, int lrow) {
-  if constexpr (KIND == kFwdGateUp) {
-    const int row = x.m0 + lrow;
-    const bool ok = row < x.hi;
-    const int I = p.Nout;
+__device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_t tacc, int quarter,
+                                         int lane, Ring& ring, const CUtensorMap* mC0,
+                                         const CUtensorMap* mC1) {
+  if constexpr (!Traits<KIND>::wgrad) {
+    const int r0 = x.m0 + quarter * 32;
+    if (r0 >= x.hi) return;  // warp-uniform: no row of this quarter is valid
+    const bool full = r0 + 32 <= x.hi;
+    const int row = r0 + lane;
+    const bool rv = row < x.hi;
+    if constexpr (KIND == kFwdGateUp) {
+      const int I = p.Nout;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t g[32], u[32];
-      tmem_ld_32x32b_x32(tacc + c * 32, g);
-      tmem_ld_32x32b_x32(tacc + 128 + c * 32, u);
-      tmem_ld_wait();
-      const int col = x.n0 + c * 32;
-      if (ok && col < I) {
-        uint32_t a[32];
+      for (int c = 0; c < 4; ++c) {
+        const int col = x.n0 + c * 32;
+        if (col >= I) break;
+        uint32_t g[32], u[32], w[16];
+        tmem_ld_32x32b_x32(tacc + c * 32, g);
+        tmem_ld_32x32b_x32(tacc + 128 + c * 32, u);
+        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-          a[j] = __float_as_uint(gv / (1.f + __expf(-gv)) * uv);
+        for (int j = 0; j < 16; ++j) {
+          const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+          const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+          w[j] = pack_bf16x2(g0 / (1.f + __expf(-g0)) * u0, g1 / (1.f + __expf(-g1)) * u1);
         }
-        store_row32(p.out + (size_t)row * I + col, a);
+        uint32_t b = ring.next(lane);
+        stage_row(b, lane, w);
+        flush_unit<false>(b, lane, full, mC0, col, r0, 0,
+                          (!full && rv) ? p.out + (size_t)row * I + col : nullptr);
         if (p.save != nullptr) {
-          store_row32(p.save + (size_t)row * 2 * I + col, g);
-          store_row32(p.save + (size_t)row * 2 * I + I + col, u);
+          pack32(g, w);
+          b = ring.next(lane);
+          stage_row(b, lane, w);
+          flush_unit<false>(b, lane, full, mC1, col, r0, 0,
+                            (!full && rv) ? p.save + (size_t)row * 2 * I + col : nullptr);
+          pack32(u, w);
+          b = ring.next(lane);
+          stage_row(b, lane, w);
+          flush_unit<false>(b, lane, full, mC1, I + col, r0, 0,
+                            (!full && rv) ? p.save + (size_t)row * 2 * I + I + col : nullptr);
         }
       }
-    }
-  } else if constexpr (KIND == kFwdDown || KIND == kDgradGateUp) {
-    const int row = x.m0 + lrow;
-    const bool ok = row < x.hi;
+    } else if constexpr (KIND == kFwdDown || KIND == kDgradGateUp) {
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(tacc + c * 32, v);
-      tmem_ld_wait();
-      const int col = x.n0 + c * 32;
-      if (ok && col < p.Nout) store_row32(p.out + (size_t)row * p.Nout + col, v);
-    }
-  } else if constexpr (KIND == kDgradDown) {
-    // dA -> SwiGLU backward with the saved pre-activations (g, u):
-    //   dg = dA * u * s * (1 + g (1 - s)),  du = dA * g * s,  s = sigmoid(g)
-    const int row = x.m0 + lrow;
-    const bool ok = row < x.hi;
-    const int I = p.I;
+      for (int c = 0; c < 8; ++c) {
+        const int col = x.n0 + c * 32;
+        if (col >= p.Nout) break;
+        uint32_t v[32], w[16];
+        tmem_ld_32x32b_x32(tacc + c * 32, v);
+        tmem_ld_wait();
+        pack32(v, w);
+        const uint32_t b = ring.next(lane);
+        stage_row(b, lane, w);
+        flush_unit<false>(b, lane, full, mC0, col, r0, 0,
+                          (!full && rv) ? p.out + (size_t)row * p.Nout + col : nullptr);
+      }
+    } else {  // kDgradDown
+      // dA -> SwiGLU backward with the saved pre-activations (g, u):
+      //   dg = dA * u * s * (1 + g (1 - s)),  du = dA * g * s,  s = sigmoid(g)
+      const int I = p.I;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(tacc + c * 32, v);
-      tmem_ld_wait();
-      const int col = x.n0 + c * 32;
-      if (ok && col < I) {
+      for (int c = 0; c < 8; ++c) {
+        const int col = x.n0 + c * 32;
+        if (col >= I) break;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + c * 32, v);
+        tmem_ld_wait();
         float g[32], u[32];
-        load_row32(p.aux + (size_t)row * 2 * I + col, g);
-        load_row32(p.aux + (size_t)row * 2 * I + I + col, u);
-        uint32_t dg[32], du[32];
+        if (rv) {
+          load_row32(p.aux + (size_t)row * 2 * I + col, g);
+          load_row32(p.aux + (size_t)row * 2 * I + I + col, u);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float da = __uint_as_float(v[j]);
-          const float s = 1.f / (1.f + __expf(-g[j]));
-          dg[j] = __float_as_uint(da * u[j] * s * (1.f + g[j] * (1.f - s)));
-          du[j] = __float_as_uint(da * g[j] * s);
+          for (int j = 0; j < 32; ++j) g[j] = u[j] = 0.f;
         }
-        store_row32(p.out + (size_t)row * 2 * I + col, dg);
-        store_row32(p.out + (size_t)row * 2 * I + I + col, du);
+        uint32_t wg[16], wu[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float dg2[2], du2[2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int k = 2 * j + q;
+            const float da = __uint_as_float(v[k]);
+            const float sg = 1.f / (1.f + __expf(-g[k]));
+            dg2[q] = da * u[k] * sg * (1.f + g[k] * (1.f - sg));
+            du2[q] = da * g[k] * sg;
+          }
+          wg[j] = pack_bf16x2(dg2[0], dg2[1]);
+          wu[j] = pack_bf16x2(du2[0], du2[1]);
+        }
+        uint32_t b = ring.next(lane);
+        stage_row(b, lane, wg);
+        flush_unit<false>(b, lane, full, mC0, col, r0, 0,
+                          (!full && rv) ? p.out + (size_t)row * 2 * I + col : nullptr);
+        b = ring.next(lane);
+        stage_row(b, lane, wu);
+        flush_unit<false>(b, lane, full, mC0, I + col, r0, 0,
+                          (!full && rv) ? p.out + (size_t)row * 2 * I + I + col : nullptr);
       }
     }
-  } else {  // wgrad
-    const int m = x.m0 + lrow;
-    const bool ok = m < p.Mout;
-    __nv_bfloat16* dst_row = nullptr;
-    if (ok) {
-      if constexpr (KIND == kWgradDown) {
-        dst_row = p.out + ((size_t)x.e * p.Mout + m) * p.Nout;
-      } else {
-        dst_row = (m < p.I) ? p.out + ((size_t)x.e * p.I + m) * p.Nout
-                            : p.out2 + ((size_t)x.e * p.I + (m - p.I)) * p.Nout;
+  } else {  // wgrad: output rows m of expert e; Mout and I are multiples of 32
+    const int r0 = x.m0 + quarter * 32;
+    if (r0 >= p.Mout) return;
+    const CUtensorMap* map = mC0;
+    int y = r0;
+    if constexpr (KIND == kWgradGateUp) {
+      if (r0 >= p.I) {
+        map = mC1;
+        y = r0 - p.I;
       }
     }
     const bool empty = x.kblocks == 0;  // uniform over the tile
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       const int col = x.n0 + c * 32;
+      if (col >= p.Nout) break;
+      uint32_t w[16];
       if (empty) {
-        if (ok && col < p.Nout) store_zero32(dst_row + col);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = 0u;
       } else {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tacc + c * 32, v);
         tmem_ld_wait();
-        if (ok && col < p.Nout) store_row32(dst_row + col, v);
+        pack32(v, w);
       }
+      const uint32_t b = ring.next(lane);
+      stage_row(b, lane, w);
+      flush_unit<true>(b, lane, true, map, col, y, x.e, nullptr);
     }
   }
 }
@@ -288,15 +389,17 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
-              const __grid_constant__ CUtensorMap mapB1, const Params p) {
+              const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapC0,
+              const __grid_constant__ CUtensorMap mapC1, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
-  const uint32_t ctrl = base + STAGES * STAGE_BYTES;
-  uint8_t* gctrl = gbase + STAGES * STAGE_BYTES;
+  const uint32_t staging = base + STAGES * STAGE_BYTES;
+  const uint32_t ctrl = staging + STAGING_BYTES;
+  uint8_t* gctrl = gbase + STAGES * STAGE_BYTES + STAGING_BYTES;
   auto full_bar = [&](int s) { return ctrl + 8u * s; };
   auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
   auto tfull_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + a); };
@@ -325,6 +428,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB0);
     tma_prefetch_desc(&mapB1);
+    tma_prefetch_desc(&mapC0);
+    tma_prefetch_desc(&mapC1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
@@ -438,7 +543,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
-    const int lrow = quarter * 32 + lane;
+    Ring ring{staging + (uint32_t)(warp - 2) * NBUF * UNIT_BYTES, 0};
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const Tile x = decode_tile<KIND>(t, p, prefix);
@@ -447,10 +552,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
-      epilogue<KIND>(x, p, tacc, lrow);
+      epilogue<KIND>(x, p, tacc, quarter, lane, ring, &mapC0, &mapC1);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
     }
+    // the CTA's stores must be complete before it exits
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -477,7 +585,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // bf16 tensor map, 128-byte swizzle; dims innermost first, strides in bytes.
-bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint32_t* box) {
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint32_t* box,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3], gstride[2];
@@ -491,14 +600,14 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, c
   }
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gdim,
                         gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 template <int KIND>
-int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
-           cudaStream_t s) {
+int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+           const CUtensorMap& c0, const CUtensorMap& c1, const Params& p, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
@@ -506,7 +615,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, c
                                 (int)SMEM_BYTES);
   });
   if (attr != cudaSuccess) return MOE_ERR_CUDA;
-  gmm_tc_kernel<KIND><<<sm_count(), kThreads, SMEM_BYTES, s>>>(a, b0, b1, p);
+  gmm_tc_kernel<KIND><<<sm_count(), kThreads, SMEM_BYTES, s>>>(a, b0, b1, c0, c1, p);
   count_launches(1);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -533,6 +642,20 @@ Params base_params(const int32_t* off, int N, int E, int32_t* status) {
 
 using namespace tc;
 
+// Store maps: units of 32 columns x 32 rows (one epilogue warp's rows),
+// 64-byte swizzle to match the staging layout.
+bool store_map_2d(CUtensorMap* m, const void* ptr, int cols, int rows) {
+  const uint64_t d[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint32_t b[2] = {32, 32};
+  return make_map(m, ptr, 2, d, b, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool store_map_3d(CUtensorMap* m, const void* ptr, int cols, int rows, int E) {
+  const uint64_t d[3] = {(uint64_t)cols, (uint64_t)rows, (uint64_t)E};
+  const uint32_t b[3] = {32, 32, 1};
+  return make_map(m, ptr, 3, d, b, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const int32_t* off,
                             int N, int H, int I, int E, void* act, void* save, int32_t* status,
                             cudaStream_t s) {
@@ -551,7 +674,10 @@ int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const
   p.n_tiles = (I + 127) / 128;
   p.out = static_cast<__nv_bfloat16*>(act);
   p.save = static_cast<__nv_bfloat16*>(save);
-  return launch<kFwdGateUp>(ma, mg, mu, p, s);
+  CUtensorMap c_act, c_save;
+  if (!store_map_2d(&c_act, act, I, N) || !store_map_2d(&c_save, save ? save : act, save ? 2 * I : I, N))
+    return MOE_ERR_CUDA;
+  return launch<kFwdGateUp>(ma, mg, mu, c_act, c_save, p, s);
 }
 
 int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int N, int H, int I,
@@ -569,7 +695,9 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   p.Nout = H;
   p.n_tiles = (H + 255) / 256;
   p.out = static_cast<__nv_bfloat16*>(out);
-  return launch<kFwdDown>(ma, md, md, p, s);
+  CUtensorMap c_out;
+  if (!store_map_2d(&c_out, out, H, N)) return MOE_ERR_CUDA;
+  return launch<kFwdDown>(ma, md, md, c_out, c_out, p, s);
 }
 
 int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* off, int N, int H,
@@ -591,7 +719,9 @@ int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* o
   p.n_tiles = (I + 255) / 256;
   p.out = static_cast<__nv_bfloat16*>(dgu);
   p.aux = static_cast<const __nv_bfloat16*>(gate_up);
-  return launch<kDgradDown>(m_dy, m_wd, m_wd, p, s);
+  CUtensorMap c_dgu;
+  if (!store_map_2d(&c_dgu, dgu, 2 * I, N)) return MOE_ERR_CUDA;
+  return launch<kDgradDown>(m_dy, m_wd, m_wd, c_dgu, c_dgu, p, s);
 }
 
 int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H, int I, int E,
@@ -613,7 +743,9 @@ int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H,
   q.Nout = H;
   q.n_tiles = (H + 255) / 256;
   q.out = static_cast<__nv_bfloat16*>(dX);
-  return launch<kDgradGateUp>(m_dgu, m_wg, m_wu, q, s);
+  CUtensorMap c_dx;
+  if (!store_map_2d(&c_dx, dX, H, N)) return MOE_ERR_CUDA;
+  return launch<kDgradGateUp>(m_dgu, m_wg, m_wu, c_dx, c_dx, q, s);
 }
 
 // With no rows at all the operand maps are never read (every tile has zero
@@ -636,7 +768,9 @@ int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, 
   p.m_tiles = (H + 127) / 128;
   p.n_tiles = (I + 255) / 256;
   p.out = static_cast<__nv_bfloat16*>(dWd);
-  return launch<kWgradDown>(m_a, m_b, m_b, p, s);
+  CUtensorMap c_dwd;
+  if (!store_map_3d(&c_dwd, dWd, I, H, E)) return MOE_ERR_CUDA;
+  return launch<kWgradDown>(m_a, m_b, m_b, c_dwd, c_dwd, p, s);
 }
 
 int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
@@ -659,7 +793,10 @@ int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off
   p.n_tiles = (H + 255) / 256;
   p.out = static_cast<__nv_bfloat16*>(dWg);
   p.out2 = static_cast<__nv_bfloat16*>(dWu);
-  return launch<kWgradGateUp>(m_a, m_b, m_b, p, s);
+  CUtensorMap c_dwg, c_dwu;
+  if (!store_map_3d(&c_dwg, dWg, H, I, E) || !store_map_3d(&c_dwu, dWu, H, I, E))
+    return MOE_ERR_CUDA;
+  return launch<kWgradGateUp>(m_a, m_b, m_b, c_dwg, c_dwu, p, s);
 }
 
 }  // namespace moe
