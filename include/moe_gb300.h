@@ -134,7 +134,7 @@ int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T,
  * The per-block expert counts live in one file-scope device array of
  * MOE_PERMUTE_STATIC_SCRATCH_INTS int32 (256 KiB) that every GPU which loads
  * this library holds until the process exits.  It is enough when
- * ceil(T*K / 2048) * E <= MOE_PERMUTE_STATIC_SCRATCH_INTS; larger problems
+ * ceil(T*K / 512) * E <= MOE_PERMUTE_STATIC_SCRATCH_INTS; larger problems
  * return MOE_ERR_CAPACITY before anything is launched.
  *   - The first call on a device looks up that device's address of the
  *     array (cudaGetSymbolAddress, with the device current); make that first

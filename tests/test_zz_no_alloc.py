@@ -44,7 +44,7 @@ def test_static_scratch_permute_matches_workspace_permute_on_consecutive_calls(l
 
 
 def test_static_scratch_permute_rejects_sizes_past_its_array(lib):
-    # ceil(T*K / 2048) * E = 128 * 1024 int32 > 65536
+    # ceil(T*K / 512) * E = 512 * 1024 int32 > 65536
     ids = torch.zeros((32768, 8), dtype=torch.int32, device=DEV)
     with pytest.raises(lib.MoeError) as e:
         lib.moe_permute_static_scratch(None, ids, 1024, 0)

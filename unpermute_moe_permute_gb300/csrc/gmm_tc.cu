@@ -11,8 +11,10 @@
 //     swizzle) into a 4-stage shared-memory ring;
 //   * warp 1 allocates 512 tensor-memory columns (two 128x256 fp32
 //     accumulators) and one thread issues tcgen05.mma (M=128, N=256, K=16);
-//   * warps 2-5 drain an accumulator with tcgen05.ld while the next tile
-//     accumulates into the other one, apply the epilogue and store bf16.
+//   * warps 2-9 (two per TMEM lane quarter, each taking half of the
+//     columns) drain an accumulator with tcgen05.ld while the next tile
+//     accumulates into the other one, apply the epilogue, stage bf16 in
+//     shared memory and write it with TMA stores.
 //
 // Six variants (KIND) share the machinery:
 //   FwdGateUp   act = silu(X Wg^T) * (X Wu^T)       B tile = 128 rows of Wg
@@ -38,7 +40,8 @@ namespace moe {
 namespace tc {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16, STAGES = 4;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half of the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;        // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -46,9 +49,9 @@ constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;   // one 64 (M/N) x 64 (K) box, 8
 constexpr uint32_t TMEM_COLS = 512;
 // Epilogue staging: each epilogue warp owns a ring of NBUF units of 32 rows x
 // 32 bf16 (2 KB, 64-byte swizzle) that TMA stores copy to global memory.
-constexpr int NBUF = 2;
+constexpr int NBUF = 1;
 constexpr uint32_t UNIT_BYTES = 32 * 64;
-constexpr uint32_t STAGING_BYTES = 4 * NBUF * UNIT_BYTES;  // 16 KB
+constexpr uint32_t STAGING_BYTES = kEpiWarps * NBUF * UNIT_BYTES;  // 16 KB
 constexpr uint32_t CTRL_BYTES = 128 + (kMaxExperts + 1) * 4 + 32 * 4;
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + CTRL_BYTES + 1024;
 static_assert(8 * (2 * STAGES + 5) <= 104, "barriers overlap the control words");
@@ -190,7 +193,7 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&f)[
 // row segments.  Units that would cross the end of an expert's rows (the next
 // expert's rows follow) are copied out by the lanes whose rows are valid
 // instead.  Every unit commits one bulk group (an empty one for the copied
-// units), so the two-unit ring is recycled by counting groups.
+// units), so the ring is recycled by counting groups.
 
 struct Ring {
   uint32_t base;  // this warp's NBUF units
@@ -254,7 +257,7 @@ __device__ __forceinline__ void flush_unit(uint32_t buf, int lane, bool tma, con
 // warp's lane quarter of the accumulator; quarter: which 32 rows.
 template <int KIND>
 __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_t tacc, int quarter,
-                                         int lane, Ring& ring, const CUtensorMap* mC0,
+                                         int half, int lane, Ring& ring, const CUtensorMap* mC0,
                                          const CUtensorMap* mC1) {
   if constexpr (!Traits<KIND>::wgrad) {
     const int r0 = x.m0 + quarter * 32;
@@ -265,7 +268,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
     if constexpr (KIND == kFwdGateUp) {
       const int I = p.Nout;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         const int col = x.n0 + c * 32;
         if (col >= I) break;
         uint32_t g[32], u[32], w[16];
@@ -276,7 +279,8 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
         for (int j = 0; j < 16; ++j) {
           const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
           const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-          w[j] = pack_bf16x2(g0 / (1.f + __expf(-g0)) * u0, g1 / (1.f + __expf(-g1)) * u1);
+          w[j] = pack_bf16x2(__fdividef(g0, 1.f + __expf(-g0)) * u0,
+                             __fdividef(g1, 1.f + __expf(-g1)) * u1);
         }
         uint32_t b = ring.next(lane);
         stage_row(b, lane, w);
@@ -297,7 +301,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
       }
     } else if constexpr (KIND == kFwdDown || KIND == kDgradGateUp) {
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 4 * half; c < 4 * half + 4; ++c) {
         const int col = x.n0 + c * 32;
         if (col >= p.Nout) break;
         uint32_t v[32], w[16];
@@ -313,20 +317,49 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
       // dA -> SwiGLU backward with the saved pre-activations (g, u):
       //   dg = dA * u * s * (1 + g (1 - s)),  du = dA * g * s,  s = sigmoid(g)
       const int I = p.I;
+      const __nv_bfloat16* gu_row = p.aux + (size_t)row * 2 * I;
+      // raw bf16 (g, u) of the current piece; the next piece's are loaded
+      // before the current one is processed
+      uint4 rg[4], ru[4];
+      auto fetch = [&](int col, uint4(&a)[4], uint4(&b)[4]) {
+        if (rv && col < I) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            a[q] = ld_v4(gu_row + col + 8 * q);
+            b[q] = ld_v4(gu_row + I + col + 8 * q);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) a[q] = b[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      fetch(x.n0 + half * 128, rg, ru);
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 4 * half; c < 4 * half + 4; ++c) {
         const int col = x.n0 + c * 32;
         if (col >= I) break;
+        uint4 ng[4], nu[4];
+        fetch(c + 1 < 4 * half + 4 ? col + 32 : I, ng, nu);
         uint32_t v[32];
         tmem_ld_32x32b_x32(tacc + c * 32, v);
         tmem_ld_wait();
         float g[32], u[32];
-        if (rv) {
-          load_row32(p.aux + (size_t)row * 2 * I + col, g);
-          load_row32(p.aux + (size_t)row * 2 * I + I + col, u);
-        } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) g[j] = u[j] = 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t gw[4] = {rg[q].x, rg[q].y, rg[q].z, rg[q].w};
+          const uint32_t uw[4] = {ru[q].x, ru[q].y, ru[q].z, ru[q].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            g[8 * q + 2 * k] = bf_lo(gw[k]);
+            g[8 * q + 2 * k + 1] = bf_hi(gw[k]);
+            u[8 * q + 2 * k] = bf_lo(uw[k]);
+            u[8 * q + 2 * k + 1] = bf_hi(uw[k]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          rg[q] = ng[q];
+          ru[q] = nu[q];
         }
         uint32_t wg[16], wu[16];
 #pragma unroll
@@ -336,7 +369,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
           for (int q = 0; q < 2; ++q) {
             const int k = 2 * j + q;
             const float da = __uint_as_float(v[k]);
-            const float sg = 1.f / (1.f + __expf(-g[k]));
+            const float sg = __fdividef(1.f, 1.f + __expf(-g[k]));
             dg2[q] = da * u[k] * sg * (1.f + g[k] * (1.f - sg));
             du2[q] = da * g[k] * sg;
           }
@@ -366,7 +399,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
     }
     const bool empty = x.kblocks == 0;  // uniform over the tile
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
       const int col = x.n0 + c * 32;
       if (col >= p.Nout) break;
       uint32_t w[16];
@@ -418,7 +451,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4 * 32);
+      mbar_init(tempty_bar(a), kEpiWarps * 32);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -541,8 +574,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
-    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    // ---------------- epilogue warps 2..9 ----------------
+    const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int half = (warp - 2) >> 2;    // which half of the tile's columns
     Ring ring{staging + (uint32_t)(warp - 2) * NBUF * UNIT_BYTES, 0};
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -552,7 +586,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
-      epilogue<KIND>(x, p, tacc, quarter, lane, ring, &mapC0, &mapC1);
+      epilogue<KIND>(x, p, tacc, quarter, half, lane, ring, &mapC0, &mapC1);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
     }

@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kSlotsPerWarp = 256;
+constexpr int kSlotsPerWarp = 64;
 constexpr int kChunk = kRouteWarps * kSlotsPerWarp;  // slots per block
 
 // Expert a slot is dispatched to, or -1: ids outside [0, E_total) and ids
@@ -58,19 +58,29 @@ route_hist_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_t
     blk_counts[(size_t)blockIdx.x * E + e] = hist[e];
 }
 
-// One block of 1024 threads: thread e owns expert e (E <= 1024).
-// In place: blk_counts[b][e] becomes the first permuted row of block b's
-// slots of expert e.
+// One block of 1024 threads.  Thread t owns expert e = t % E and the p-th of
+// P = 1024 / E ranges of blocks (E <= 1024).  In place: blk_counts[b][e]
+// becomes the first permuted row of block b's slots of expert e.
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ blk, int nblk, int E, int32_t* __restrict__ tokens_per_expert,
                   int32_t* __restrict__ expert_offsets) {
+  __shared__ int32_t part[1024];  // [P][E] partial counts, then partial bases
   __shared__ int32_t warp_tot[32];
-  const int e = threadIdx.x;
-  const int lane = e & 31, warp = e >> 5;
+  const int tid = threadIdx.x;
+  const int P = 1024 / E;
+  const int e = tid % E, pi = tid / E;
+  const bool active = pi < P;
+  const int b_lo = active ? (int)((long long)nblk * pi / P) : 0;
+  const int b_hi = active ? (int)((long long)nblk * (pi + 1) / P) : 0;
+  int psum = 0;
+  for (int b = b_lo; b < b_hi; ++b) psum += blk[(size_t)b * E + e];
+  if (active) part[pi * E + e] = psum;
+  __syncthreads();
+  // totals per expert and their exclusive scan (thread e < E)
+  const int lane = tid & 31, warp = tid >> 5;
   int cnt = 0;
-  if (e < E)
-    for (int b = 0; b < nblk; ++b) cnt += blk[(size_t)b * E + e];
-  // block-wide exclusive scan of cnt
+  if (tid < E)
+    for (int q = 0; q < P; ++q) cnt += part[q * E + tid];
   int incl = cnt;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -89,13 +99,23 @@ route_scan_kernel(int32_t* __restrict__ blk, int nblk, int E, int32_t* __restric
     warp_tot[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  const int excl = incl - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
-  if (e < E) {
-    tokens_per_expert[e] = cnt;
-    expert_offsets[e] = excl;
-    if (e == E - 1) expert_offsets[E] = excl + cnt;
+  if (tid < E) {
+    const int excl = incl - cnt + (warp > 0 ? warp_tot[warp - 1] : 0);
+    tokens_per_expert[tid] = cnt;
+    expert_offsets[tid] = excl;
+    if (tid == E - 1) expert_offsets[E] = excl + cnt;
+    // partial bases: the expert's offset plus the ranges before each range
     int run = excl;
-    for (int b = 0; b < nblk; ++b) {
+    for (int q = 0; q < P; ++q) {
+      const int c = part[q * E + tid];
+      part[q * E + tid] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (active) {
+    int run = part[pi * E + e];
+    for (int b = b_lo; b < b_hi; ++b) {
       const int c = blk[(size_t)b * E + e];
       blk[(size_t)b * E + e] = run;
       run += c;
@@ -113,13 +133,17 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wbase = blockIdx.x * kChunk + warp * kSlotsPerWarp;
   int32_t* my = cnt + warp * E;
-  // 1. per-warp counts
-  for (int i = 0; i < kSlotsPerWarp; i += 32) {
-    const int f = wbase + i + lane;
+  // 1. per-warp counts; each lane keeps the experts of its slots for step 3
+  constexpr int kSteps = kSlotsPerWarp / 32;
+  int ex[kSteps];
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
+    const int f = wbase + i * 32 + lane;
+    ex[i] = -1;
     if (f < TK) {
       bool bad;
-      const int e = slot_expert(ids, f, K, E, E_total, &bad);
-      if (e >= 0) atomicAdd(&my[e], 1);
+      ex[i] = slot_expert(ids, f, K, E, E_total, &bad);
+      if (ex[i] >= 0) atomicAdd(&my[ex[i]], 1);
     }
   }
   __syncthreads();
@@ -135,13 +159,10 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int 
   __syncthreads();
   // 3. stable rank inside each 32-slot step: peers with the same expert and a
   //    lower lane come first; the step's leader advances the warp's base.
-  for (int i = 0; i < kSlotsPerWarp; i += 32) {
-    const int f = wbase + i + lane;
-    int e = -1;
-    if (f < TK) {
-      bool bad;
-      e = slot_expert(ids, f, K, E, E_total, &bad);
-    }
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
+    const int f = wbase + i * 32 + lane;
+    const int e = ex[i];
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lanemask_lt());
     if (e >= 0) {
