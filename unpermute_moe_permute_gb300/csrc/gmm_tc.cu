@@ -39,7 +39,7 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, UK = 16, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half of the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KB
@@ -49,13 +49,9 @@ constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;   // one 64 (M/N) x 64 (K) box, 8
 constexpr uint32_t TMEM_COLS = 512;
 // Epilogue staging: each epilogue warp owns a ring of NBUF units of 32 rows x
 // 32 bf16 (2 KB, 64-byte swizzle) that TMA stores copy to global memory.
-constexpr int NBUF = 1;
 constexpr uint32_t UNIT_BYTES = 32 * 64;
-constexpr uint32_t STAGING_BYTES = kEpiWarps * NBUF * UNIT_BYTES;  // 16 KB
 constexpr uint32_t CTRL_BYTES = 128 + (kMaxExperts + 1) * 4 + 32 * 4;
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + CTRL_BYTES + 1024;
-static_assert(8 * (2 * STAGES + 5) <= 104, "barriers overlap the control words");
-static_assert(SMEM_BYTES <= 232448, "more shared memory than one CTA may use");
+constexpr int kMaxStages = 4;
 
 enum Kind : int {
   kFwdGateUp = 0,
@@ -73,6 +69,21 @@ struct Traits {
   static constexpr bool wgrad = (KIND == kWgradDown || KIND == kWgradGateUp);
   static constexpr int n_per_tile = (KIND == kFwdGateUp) ? 128 : 256;  // output columns
   static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
+  // Every kind is fed through the load pipeline (measured: a fourth stage
+  // beats a second staging unit per epilogue warp for all six).
+  static constexpr int stages = 4;
+  static constexpr int nbuf = 1;
+  // Cluster size.  With cs = 2, CTA pairs take vertically adjacent 128-row
+  // tiles that share their B tile: each CTA loads half of B and multicasts
+  // it to both (32 KB instead of 48 KB from L2 per CTA and k block).  On
+  // GB300 that measured slower for all six kinds at the benchmark shapes
+  // (the pair runs in lockstep and fewer SMs hold whole clusters), so
+  // single CTAs are used.
+  static constexpr int cs = 1;
+  static constexpr uint32_t staging_bytes = kEpiWarps * nbuf * UNIT_BYTES;
+  static constexpr uint32_t smem_bytes = stages * STAGE_BYTES + staging_bytes + CTRL_BYTES + 1024;
+  static_assert(8 * (2 * stages + 5) <= 104, "barriers overlap the control words");
+  static_assert(smem_bytes <= 232448, "more shared memory than one CTA may use");
 };
 
 struct Params {
@@ -98,65 +109,89 @@ struct Tile {
   int kblocks;    // 64-deep k blocks
 };
 
+// Cluster tile t: a group of CS vertically adjacent 128-row tiles of one
+// expert and one n tile; this CTA (cluster rank `rank`) takes the rank-th.
+// A rank whose rows lie past the expert's end computes a tile that is never
+// stored (its loads read the next expert's rows, or zeros past the buffer).
 template <int KIND>
-__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_t* prefix) {
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_t* prefix,
+                                            int rank) {
+  constexpr int CS = Traits<KIND>::cs;
   Tile x;
   if constexpr (!Traits<KIND>::wgrad) {
-    const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
-    const int e = find_expert(prefix, p.E, mt);
+    const int mg = t / p.n_tiles, nt = t - mg * p.n_tiles;
+    const int e = find_expert(prefix, p.E, mg);
     const ExpertRows r = expert_rows(p.off, e, p.N);
     x.e = e;
     x.lo = r.lo;
     x.hi = r.hi;
-    x.m0 = r.lo + (mt - prefix[e]) * BM;
+    x.m0 = r.lo + (mg - prefix[e]) * (BM * CS) + rank * BM;
     x.n0 = nt * Traits<KIND>::n_per_tile;
     x.kblocks = p.Kd / BK;
   } else {
-    const int per = p.m_tiles * p.n_tiles;
+    const int m_groups = (p.m_tiles + CS - 1) / CS;
+    const int per = m_groups * p.n_tiles;
     const int e = t / per, rem = t - e * per;
-    const int mt = rem / p.n_tiles, nt = rem - mt * p.n_tiles;
+    const int mg = rem / p.n_tiles, nt = rem - mg * p.n_tiles;
     const ExpertRows r = expert_rows(p.off, e, p.N);
     x.e = e;
     x.lo = r.lo;
     x.hi = r.hi;
-    x.m0 = mt * BM;
+    x.m0 = (mg * CS + rank) * BM;
     x.n0 = nt * BN;
     x.kblocks = (r.hi - r.lo + BK - 1) / BK;
   }
   return x;
 }
 
-// TMA loads of k block kb of tile x into one stage.
+// TMA loads of k block kb of tile x into one stage.  A is this CTA's own.
+// B is shared by the cluster: with CS = 2 this CTA loads half of it (one of
+// the two 128-row K-major boxes, or two of the four 64-column MN-major
+// boxes) and multicasts it into both CTAs.
 template <int KIND>
 __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& p, uint32_t sa,
                                            uint32_t sb, uint32_t bar, const CUtensorMap* mA,
-                                           const CUtensorMap* mB0, const CUtensorMap* mB1) {
+                                           const CUtensorMap* mB0, const CUtensorMap* mB1,
+                                           int rank) {
+  constexpr int CS = Traits<KIND>::cs;
+  constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
   const int k0 = kb * BK;
+  auto b3 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by, int bz) {
+    if constexpr (CS > 1) tma_load_3d_mc(dst, m, bar, bx, by, bz, kMask);
+    else tma_load_3d(dst, m, bar, bx, by, bz);
+  };
+  auto b2 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by) {
+    if constexpr (CS > 1) tma_load_2d_mc(dst, m, bar, bx, by, kMask);
+    else tma_load_2d(dst, m, bar, bx, by);
+  };
+  // which of the B boxes this CTA loads: K-major B has 2, MN-major B has 4
+  constexpr int kBoxes = Traits<KIND>::b_mn ? 4 : 2;
+  constexpr int kMine = kBoxes / CS;
+  const int j0 = rank * kMine;
   if constexpr (KIND == kFwdGateUp) {
     tma_load_2d(sa, mA, bar, k0, x.m0);
-    tma_load_3d(sb, mB0, bar, k0, x.n0, x.e);
-    tma_load_3d(sb + B_BYTES / 2, mB1, bar, k0, x.n0, x.e);
+#pragma unroll
+    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * (B_BYTES / 2), j == 0 ? mB0 : mB1, k0, x.n0, x.e);
   } else if constexpr (KIND == kFwdDown) {
     tma_load_2d(sa, mA, bar, k0, x.m0);
-    tma_load_3d(sb, mB0, bar, k0, x.n0, x.e);
-    tma_load_3d(sb + B_BYTES / 2, mB0, bar, k0, x.n0 + 128, x.e);
+#pragma unroll
+    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * (B_BYTES / 2), mB0, k0, x.n0 + 128 * j, x.e);
   } else if constexpr (KIND == kDgradDown) {
     tma_load_2d(sa, mA, bar, k0, x.m0);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * MN_BOX_BYTES, mB0, bar, x.n0 + j * 64, k0, x.e);
+    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * MN_BOX_BYTES, mB0, x.n0 + j * 64, k0, x.e);
   } else if constexpr (KIND == kDgradGateUp) {
     tma_load_2d(sa, mA, bar, k0, x.m0);
     const bool up = k0 >= p.I;
     const int kk = up ? k0 - p.I : k0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      tma_load_3d(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, bar, x.n0 + j * 64, kk, x.e);
+    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, x.n0 + j * 64, kk, x.e);
   } else {  // wgrad: both operands MN-major, k = token rows of the expert
     const int row = x.lo + k0;
 #pragma unroll
     for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * MN_BOX_BYTES, mA, bar, x.m0 + j * 64, row);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * MN_BOX_BYTES, mB0, bar, x.n0 + j * 64, row);
+    for (int j = j0; j < j0 + kMine; ++j) b2(sb + j * MN_BOX_BYTES, mB0, x.n0 + j * 64, row);
   }
 }
 
@@ -195,6 +230,7 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float (&f)[
 // instead.  Every unit commits one bulk group (an empty one for the copied
 // units), so the ring is recycled by counting groups.
 
+template <int NBUF>
 struct Ring {
   uint32_t base;  // this warp's NBUF units
   int slot;       // next unit to fill
@@ -257,7 +293,8 @@ __device__ __forceinline__ void flush_unit(uint32_t buf, int lane, bool tma, con
 // warp's lane quarter of the accumulator; quarter: which 32 rows.
 template <int KIND>
 __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_t tacc, int quarter,
-                                         int half, int lane, Ring& ring, const CUtensorMap* mC0,
+                                         int half, int lane, Ring<Traits<KIND>::nbuf>& ring,
+                                         const CUtensorMap* mC0,
                                          const CUtensorMap* mC1) {
   if constexpr (!Traits<KIND>::wgrad) {
     const int r0 = x.m0 + quarter * 32;
@@ -424,6 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
               const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapC0,
               const __grid_constant__ CUtensorMap mapC1, const Params p) {
+  constexpr int STAGES = Traits<KIND>::stages;
+  constexpr int NBUF = Traits<KIND>::nbuf;
+  constexpr int CS = Traits<KIND>::cs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -431,8 +471,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
   const uint32_t staging = base + STAGES * STAGE_BYTES;
-  const uint32_t ctrl = staging + STAGING_BYTES;
-  uint8_t* gctrl = gbase + STAGES * STAGE_BYTES + STAGING_BYTES;
+  const uint32_t ctrl = staging + Traits<KIND>::staging_bytes;
+  uint8_t* gctrl = gbase + STAGES * STAGE_BYTES + Traits<KIND>::staging_bytes;
   auto full_bar = [&](int s) { return ctrl + 8u * s; };
   auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
   auto tfull_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + a); };
@@ -447,7 +487,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CS);  // released by the MMA of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -471,26 +511,32 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   int total;
   if constexpr (Traits<KIND>::wgrad) {
     __syncthreads();
-    total = p.E * p.m_tiles * p.n_tiles;
+    total = p.E * ((p.m_tiles + CS - 1) / CS) * p.n_tiles;
   } else {
-    build_tile_prefix(p.off, p.E, p.N, BM, prefix, scratch);  // ends with __syncthreads
+    build_tile_prefix(p.off, p.E, p.N, BM * CS, prefix, scratch);  // ends with __syncthreads
     total = prefix[p.E] * p.n_tiles;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // The peer's multicasts and commits target this CTA's barriers: they must
+  // all be initialised cluster-wide first.
+  if constexpr (CS > 1) cluster_sync_all();
+  const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
+  const int t_first = CS > 1 ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int t_step = CS > 1 ? (int)cluster_count_x() : (int)gridDim.x;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int issued[STAGES];
+      int issued[kMaxStages];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) issued[s] = -1;
       int g = 0;
       bool run = true;
-      for (int t = blockIdx.x; run && t < total; t += gridDim.x) {
-        const Tile x = decode_tile<KIND>(t, p, prefix);
+      for (int t = t_first; run && t < total; t += t_step) {
+        const Tile x = decode_tile<KIND>(t, p, prefix, rank);
         for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1;
@@ -500,7 +546,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           }
           mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
           load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, full_bar(s), &mapA,
-                           &mapB0, &mapB1);
+                           &mapB0, &mapB1, rank);
           issued[s] = (int)ph;
         }
       }
@@ -513,8 +559,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // ---------------- MMA issuer ----------------
     int g = 0, it = 0;
     bool run = true;
-    for (int t = blockIdx.x; run && t < total; t += gridDim.x, ++it) {
-      const Tile x = decode_tile<KIND>(t, p, prefix);
+    for (int t = t_first; run && t < total; t += t_step, ++it) {
+      const Tile x = decode_tile<KIND>(t, p, prefix, rank);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
@@ -560,7 +606,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
                                                    : desc_sw128(sb + kk * (UK * 2), 16, 1024);
             umma_f16(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(empty_bar(s));
+          if constexpr (CS > 1) umma_commit_mc(empty_bar(s), (uint16_t)((1u << CS) - 1u));
+          else umma_commit(empty_bar(s));
         }
         __syncwarp();
       }
@@ -577,10 +624,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // ---------------- epilogue warps 2..9 ----------------
     const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
-    Ring ring{staging + (uint32_t)(warp - 2) * NBUF * UNIT_BYTES, 0};
+    Ring<NBUF> ring{staging + (uint32_t)(warp - 2) * NBUF * UNIT_BYTES, 0};
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile x = decode_tile<KIND>(t, p, prefix);
+    for (int t = t_first; t < total; t += t_step, ++it) {
+      const Tile x = decode_tile<KIND>(t, p, prefix, rank);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))) break;
@@ -596,6 +643,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  // No CTA leaves while its peer may still signal its barriers.
+  if constexpr (CS > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -646,12 +695,39 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
     attr = cudaFuncSetAttribute(gmm_tc_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)SMEM_BYTES);
+                                (int)Traits<KIND>::smem_bytes);
   });
   if (attr != cudaSuccess) return MOE_ERR_CUDA;
-  gmm_tc_kernel<KIND><<<sm_count(), kThreads, SMEM_BYTES, s>>>(a, b0, b1, c0, c1, p);
+  constexpr int CS = Traits<KIND>::cs;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Traits<KIND>::smem_bytes;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  // one persistent CTA per SM, as many whole clusters as can be resident
+  int clusters = sm_count() / CS;
+  static int resident = -1;
+  if (resident < 0) {
+    cfg.gridDim = dim3(clusters * CS, 1, 1);
+    int n = 0;
+    resident = (cudaOccupancyMaxActiveClusters(&n, gmm_tc_kernel<KIND>, &cfg) == cudaSuccess && n > 0)
+                   ? n
+                   : 0;
+    (void)cudaGetLastError();
+  }
+  if (resident > 0 && resident < clusters) clusters = resident;
+  cfg.gridDim = dim3(clusters * CS, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, gmm_tc_kernel<KIND>, a, b0, b1, c0, c1, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
   count_launches(1);
-  MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
 
