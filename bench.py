@@ -90,6 +90,12 @@ def reduce_max(value: float, device) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_step: int, steps: int, world: int, max_elapsed_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (weak scaling: each rank runs its own batch)."""
+    return units_per_step * steps * world / (max_elapsed_ms / 1e3)
+
+
 def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -616,8 +622,7 @@ def run_ours(args, world, rank, local):
     barrier()
     elapsed_ms = start.elapsed_time(end)
     max_ms = reduce_max(elapsed_ms, dev)
-    units = work.units_per_step * args.steps * world
-    value = units / (max_ms / 1e3)
+    value = job_throughput(work.units_per_step, args.steps, world, max_ms)
 
     # per-kernel figures and the dominant kernel
     per = timers.summary()
