@@ -153,6 +153,18 @@ int moe_permute_static_scratch(const void* tokens, int dtype, const int32_t* exp
                                int32_t* tokens_per_expert, int32_t* expert_offsets,
                                int32_t* dev_status, cudaStream_t stream);
 
+/* moe_permute with an activity mask (the x_active_mask parameter of the
+ * torch_npu npu_moe_distribute_combine_v2 API reference): mask_dims 1 =
+ * active_mask [T] (one byte per token), 2 = active_mask [T, K] (one byte per
+ * slot); a zero byte means the token / slot takes no part, so it is not
+ * dispatched (row_map = -1, not counted).  Ids of masked slots are still
+ * validated.  active_mask NULL = every slot active (moe_permute). */
+int moe_permute_masked(const void* tokens, int dtype, const int32_t* expert_ids, int T, int H,
+                       int K, int E, int num_special, const uint8_t* active_mask, int mask_dims,
+                       void* permuted, int32_t* sorted_indices, int32_t* row_map,
+                       int32_t* tokens_per_expert, int32_t* expert_offsets, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
 /* Rebuild row_map [TK] from sorted_indices [N] (row_map[sorted[i]] = i,
  * every other entry -1).  For callers that keep only sorted_indices. */
 int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, int TK, int32_t* row_map,
@@ -230,6 +242,16 @@ int moe_combine(const void* expanded, int dtype, const int32_t* row_map, const i
                 const void* alpha2, const void* const_v, void* out, int32_t* dev_status,
                 cudaStream_t stream);
 
+/* moe_combine with the activity mask of moe_permute_masked: a slot (or every
+ * slot of a token) masked off contributes nothing to the weighted sum; the
+ * shared-expert term is still added.  active_mask NULL = moe_combine. */
+int moe_combine_masked(const void* expanded, int dtype, const int32_t* row_map,
+                       const int32_t* expert_ids, const float* scales, const void* shared_x,
+                       const void* ori_x, const uint8_t* active_mask, int mask_dims, int T, int H,
+                       int K, int N, int E, int zero_num, int copy_num, int const_num,
+                       const void* alpha1, const void* alpha2, const void* const_v, void* out,
+                       int32_t* dev_status, cudaStream_t stream);
+
 /* ---- rank-major -> expert-major permute indices (hyper_parallel
  * expert_parallel.py, _generate_permute_indices) -----------------------------
  *
@@ -246,6 +268,23 @@ int moe_combine(const void* expanded, int dtype, const int32_t* row_map, const i
 int moe_permute_indices(const int32_t* counts, int R, int E, int32_t* indices, int capacity,
                         int32_t* tokens_per_expert, int32_t* total, int32_t* dev_status,
                         cudaStream_t stream);
+
+/* Deredundancy dispatch indices (hyper_parallel expert_parallel.py,
+ * _generate_deredundency_dispatch_indices): counts [R, E_all] row-major, entry
+ * r*E_all+e = rows that source r holds for expert e; the source buffer is the
+ * sources' expert-major buffers concatenated, i.e. blocks in (r, e) order.
+ * For the window of experts [col_start, col_start + col_count) (an outer
+ * expert range: iep_size * num_local_experts experts) the output visits
+ * blocks column-major (e = col_start.., then r = 0..R-1), i.e. ordered
+ * [destination, local expert, source]:
+ *   indices[i] = source position of destination i,  i < *total
+ *   tokens_per_column[c] = sum_r counts[r*E_all + col_start + c]
+ * moe_permute_indices is the full window (col_start 0, col_count E).
+ * Same limits and capacity behaviour as moe_permute_indices (R*E_all <= 2048). */
+int moe_permute_indices_window(const int32_t* counts, int R, int E_all, int col_start,
+                               int col_count, int32_t* indices, int capacity,
+                               int32_t* tokens_per_column, int32_t* total, int32_t* dev_status,
+                               cudaStream_t stream);
 
 /* ---- expert MLP backward (bf16) -----------------------------------------
  *

@@ -66,6 +66,7 @@ __all__ = [
     "unpermute_grad",
     "combine",
     "permute_indices",
+    "deredundancy_dispatch_indices",
     "permute_grad",
     "expert_mlp_grad",
 ]
@@ -142,7 +143,20 @@ def validate_expert_ids(expert_ids, num_experts: int, num_special: int = 0):
             raise ValueError(f"row {t} repeats an expert id")
 
 
-def permute_routing(expert_ids, num_experts: int, num_special: int = 0):
+def _active(active_mask, T: int, K: int):
+    """[CMB] ``x_active_mask``: [T] per token or [T, K] per slot; None = all
+    active.  Returns a flat [T*K] bool array."""
+    if active_mask is None:
+        return np.ones(T * K, dtype=bool)
+    m = np.asarray(active_mask).astype(bool)
+    if m.shape == (T,):
+        m = np.repeat(m, K)
+    elif m.shape != (T, K):
+        raise ValueError("active mask must be [T] or [T, K]")
+    return m.reshape(-1)
+
+
+def permute_routing(expert_ids, num_experts: int, num_special: int = 0, active_mask=None):
     """Expert-major routing of the T*K slots ([EP] ``_generate_permute_indices``
     docstring: the expert-major buffer holds all rows of expert 0, then all of
     expert 1, ...; readings R2, R3, R9).
@@ -153,10 +167,13 @@ def permute_routing(expert_ids, num_experts: int, num_special: int = 0):
       expert_offsets       = exclusive prefix sum of tokens_per_expert
       sorted_indices       = stable argsort of the flat ids (dispatched slots)
       row_map[f]           = position of slot f in the permuted buffer, or -1
+    A slot masked off by ``active_mask`` ([CMB] ``x_active_mask``) takes no
+    part: it is not dispatched.
     """
     validate_expert_ids(expert_ids, num_experts, num_special)
+    T, K = np.asarray(expert_ids).shape
     flat = np.asarray(expert_ids, dtype=np.int64).reshape(-1)
-    dispatched = np.nonzero(flat < num_experts)[0]
+    dispatched = np.nonzero((flat < num_experts) & _active(active_mask, T, K))[0]
     order = np.argsort(flat[dispatched], kind="stable")
     sorted_indices = dispatched[order].astype(np.int64)
     tokens_per_expert = np.bincount(flat[dispatched], minlength=num_experts).astype(np.int64)
@@ -275,7 +292,7 @@ def unpermute_grad(grad_out, permuted_tokens, row_map, probs, T: int, K: int, dt
 
 def combine(expanded, row_map, expert_ids, scales, shared_x, ori_x, num_experts: int,
             zero_num: int, copy_num: int, const_num: int,
-            alpha1, alpha2, const_v, dtype: str):
+            alpha1, alpha2, const_v, dtype: str, active_mask=None):
     """[CMB] function description: x = Sum_k(expert_scales * y_k) + shared_expert_x,
 
     where y_k, the expert output for slot (t, k) with id e, is
@@ -286,6 +303,8 @@ def combine(expanded, row_map, expert_ids, scales, shared_x, ori_x, num_experts:
                                                                   (const expert)
     The id ranges follow [CMB] ``zero_expert_num`` / ``copy_expert_num`` /
     ``const_expert_num``.  Readings R4, R5, R6.  shared_x None adds nothing.
+    A slot masked off by ``active_mask`` ([CMB] ``x_active_mask``) adds
+    nothing (reading R18); the shared term is still added.
     """
     ids = np.asarray(expert_ids, dtype=np.int64)
     T, K = ids.shape
@@ -302,10 +321,13 @@ def combine(expanded, row_map, expert_ids, scales, shared_x, ori_x, num_experts:
     copy_lo = zero_lo + zero_num
     const_lo = copy_lo + copy_num
     const_hi = const_lo + const_num
+    act = _active(active_mask, T, K).reshape(T, K)
     x = np.zeros((T, H))
     for t in range(T):
         acc = np.zeros(H)
         for k in range(K):
+            if not act[t, k]:
+                continue
             e = ids[t, k]
             if e < zero_lo:
                 y = Y[rm[t, k]]
@@ -363,6 +385,47 @@ def permute_indices(counts, num_ranks: int, experts_per_rank: int):
     tokens_per_expert = np.array([sum(int(c[r * E + e]) for r in range(R)) for e in range(E)],
                                  dtype=np.int64)
     return np.array(out, dtype=np.int64), tokens_per_expert, len(out)
+
+
+def deredundancy_dispatch_indices(counts, expert_start: int, iep_size: int,
+                                  num_local_experts: int):
+    """[EP] ``_generate_deredundency_dispatch_indices``.
+
+    ``counts[o, e]`` rows of expert e sit in source o's expert-major buffer;
+    the sources' buffers are concatenated (source 0 first), so block (o, e)
+    starts after every block (o', e') that precedes it in (o, e) order.  The
+    output selects the outer expert range [expert_start, expert_start +
+    iep_size * num_local_experts) and orders its rows as [iep destination d,
+    local expert l, source o] (expert e = expert_start + d * L + l), each
+    block keeping its rows in order.  Also returns, per (d, l), the rows of
+    that expert summed over the sources.
+    """
+    c = np.asarray(counts, dtype=np.int64)
+    if c.ndim != 2:
+        raise ValueError("counts must be [sources, experts]")
+    O, NE = c.shape
+    L, D = int(num_local_experts), int(iep_size)
+    if expert_start < 0 or expert_start + D * L > NE:
+        raise ValueError("expert range outside the experts")
+    if c.size and c.min() < 0:
+        raise ValueError("negative count")
+    start = np.zeros((O, NE), dtype=np.int64)
+    running = 0
+    for o in range(O):
+        for e in range(NE):
+            start[o, e] = running
+            running += int(c[o, e])
+    out = []
+    per_dest_expert = []
+    for d in range(D):
+        for l in range(L):
+            e = expert_start + d * L + l
+            n = 0
+            for o in range(O):
+                out.extend(range(int(start[o, e]), int(start[o, e] + c[o, e])))
+                n += int(c[o, e])
+            per_dest_expert.append(n)
+    return np.array(out, dtype=np.int64), np.array(per_dest_expert, dtype=np.int64), len(out)
 
 
 # --------------------------------------------------------------------------

@@ -40,7 +40,7 @@ ROUTING_CASES = [
     (1, 1, 1, 0),
     (3, 2, 4, 0),
     (100, 8, 64, 0),
-    (2049, 3, 17, 0),        # 6147 slots: three 2048-slot blocks, ragged tail
+    (2049, 3, 17, 0),        # 6147 slots: twelve 512-slot blocks and a ragged tail
     (5000, 8, 256, 12),      # special ids are not dispatched
     (777, 16, 1024, 0),      # K and E at their limits
     (300, 4, 8, 8),
@@ -308,3 +308,60 @@ def test_index_and_combine_full_size(lib):
                      np64(d["ori_x"]), E, Z, C, Cn, np64(d["alpha1"]), np64(d["alpha2"]),
                      np64(d["const_v"]), "bf16")
     assert_normwise(np64(out), want, BF16_TOL, "combine full")
+
+
+# ---------------------------------------------------------------- deredundancy indices
+
+@pytest.mark.parametrize("nsrc,NE,start,D,L,lam", [(2, 4, 2, 1, 2, 2.0), (8, 256, 64, 4, 16, 8.0),
+                                                   (3, 40, 0, 5, 8, 1.0), (8, 256, 0, 1, 1, 0.0),
+                                                   (16, 128, 120, 2, 4, 64.0)])
+def test_deredundancy_indices_bit_exact(lib, nsrc, NE, start, D, L, lam):
+    rng = np.random.Generator(np.random.PCG64(nsrc * 1000 + NE + start))
+    counts = rng.poisson(lam, size=(nsrc, NE)).astype(np.int32)
+    want_idx, want_n, want_total = O.deredundancy_dispatch_indices(counts, start, D, L)
+    st = lib.new_status()
+    idx, n, total = lib.moe_permute_indices_window(torch.from_numpy(counts.reshape(-1)).to(DEV), nsrc,
+                                                   NE, start, D * L, max(want_total, 1),
+                                                   dev_status=st)
+    assert lib.moe_check_status(st) == lib.MOE_OK
+    assert int(total.item()) == want_total
+    assert np.array_equal(np64(idx)[:want_total], want_idx)
+    assert np.array_equal(np64(n)[:D * L], want_n)
+
+
+def test_full_window_equals_permute_indices(lib):
+    rng = np.random.Generator(np.random.PCG64(9))
+    counts = torch.from_numpy(rng.poisson(5.0, 12 * 20).astype(np.int32)).to(DEV)
+    a, na, ta = lib.moe_permute_indices(counts, 12, 20, 12 * 20 * 20)
+    b, nb, tb = lib.moe_permute_indices_window(counts, 12, 20, 0, 20, 12 * 20 * 20)
+    n = int(ta.item())
+    assert n == int(tb.item()) and torch.equal(a[:n], b[:n]) and torch.equal(na, nb[:20])
+
+
+# ---------------------------------------------------------------- activity mask
+
+@pytest.mark.parametrize("dims", [1, 2])
+def test_masked_permute_and_combine(lib, dims):
+    d = moe_inputs.index_combine(3, R=1, E_local=32, T=700, H=128, K=8, zero_num=2, copy_num=2,
+                                 const_num=2)
+    T, K, E = d["T"], d["K"], d["E"]
+    ids = d["expert_ids"]
+    rng = np.random.default_rng(dims)
+    mask = rng.random(T) < 0.7 if dims == 1 else rng.random((T, K)) < 0.7
+    mask_t = torch.from_numpy(mask).to(DEV)
+    si, rm, tpe, off = O.permute_routing(ids.numpy(), E, 6, active_mask=mask)
+    tok = torch.from_numpy(rng.standard_normal((T, 128)).astype(np.float32)).bfloat16()
+    r = lib.moe_permute(tok.to(DEV), ids.to(DEV), E, 6, active_mask=mask_t)
+    assert np.array_equal(np64(r.row_map), rm)
+    assert np.array_equal(np64(r.expert_offsets), off)
+    assert np.array_equal(np64(r.permuted)[: len(si)], O.permute_rows(np64(tok), si, K))
+    expanded = torch.from_numpy(rng.standard_normal((max(len(si), 1), 128)).astype(np.float32)).bfloat16()[: len(si)]
+    out = lib.moe_combine(expanded.to(DEV).contiguous(), r.row_map, ids.to(DEV), d["scales"].to(DEV), E,
+                          shared_x=d["shared_x"].to(DEV), ori_x=d["ori_x"].to(DEV), zero_num=2,
+                          copy_num=2, const_num=2, alpha1=d["alpha1"].to(DEV),
+                          alpha2=d["alpha2"].to(DEV), const_v=d["const_v"].to(DEV),
+                          active_mask=mask_t)
+    want = O.combine(np64(expanded), rm, ids.numpy(), d["scales"].numpy(), np64(d["shared_x"]),
+                     np64(d["ori_x"]), E, 2, 2, 2, np64(d["alpha1"]), np64(d["alpha2"]),
+                     np64(d["const_v"]), "bf16", active_mask=mask)
+    assert_normwise(np64(out), want, BF16_TOL, "masked combine")

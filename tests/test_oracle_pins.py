@@ -518,3 +518,89 @@ def test_input_generators_shapes_and_routing_rules():
     a = moe_inputs.permute_unpermute(3, T=8, H=16, E=8, K=2)
     b = moe_inputs.permute_unpermute(3, T=8, H=16, E=8, K=2)
     assert torch.equal(a["tokens"], b["tokens"]) and torch.equal(a["expert_ids"], b["expert_ids"])
+
+
+# ---------------------------------------------------------------- deredundancy indices
+
+def test_deredundancy_indices_docstring_case():
+    (nsrc, NE, s, D, L), counts, want, want_n = _read_rows("deredundancy_indices_case.txt")
+    idx, n, total = O.deredundancy_dispatch_indices(np.array(counts).reshape(nsrc, NE), s, D, L)
+    assert idx.tolist() == want and n.tolist() == want_n and total == len(want)
+
+
+def _brute_deredundancy(counts, start, D, L):
+    """Label every source row with (d, l, o) if its expert is in the range,
+    then stable-sort the labelled rows by that key."""
+    nsrc, NE = counts.shape
+    labels = []
+    pos = 0
+    for o in range(nsrc):
+        for e in range(NE):
+            for _ in range(int(counts[o, e])):
+                if start <= e < start + D * L:
+                    d, l = divmod(e - start, L)
+                    labels.append(((d, l, o), pos))
+                pos += 1
+    return [p for _, p in sorted(labels, key=lambda kv: kv[0])]
+
+
+@pytest.mark.parametrize("nsrc,NE,start,D,L", [(1, 1, 0, 1, 1), (3, 8, 2, 2, 3), (4, 16, 0, 4, 4),
+                                               (8, 32, 16, 4, 4), (2, 5, 4, 1, 1)])
+def test_deredundancy_indices_brute_force(nsrc, NE, start, D, L):
+    rng = np.random.default_rng(nsrc * 7 + NE)
+    counts = rng.poisson(2.0, size=(nsrc, NE))
+    idx, n, total = O.deredundancy_dispatch_indices(counts, start, D, L)
+    assert idx.tolist() == _brute_deredundancy(counts, start, D, L)
+    assert n.tolist() == [int(counts[:, start + j].sum()) for j in range(D * L)]
+    assert total == len(idx)
+
+
+def test_deredundancy_full_range_is_the_rank_to_expert_permutation():
+    """With the whole expert range the deredundancy order (expert, source)
+    is the rank-major -> expert-major permutation of the same counts."""
+    rng = np.random.default_rng(5)
+    counts = rng.poisson(3.0, size=(4, 6))
+    a, na, ta = O.deredundancy_dispatch_indices(counts, 0, 2, 3)
+    b, nb, tb = O.permute_indices(counts.reshape(-1), 4, 6)
+    assert a.tolist() == b.tolist() and na.tolist() == nb.tolist() and ta == tb
+
+
+# ---------------------------------------------------------------- activity mask
+
+def test_masked_routing_brute_force_and_token_mask_broadcast():
+    rng = np.random.default_rng(21)
+    T, K, E = 9, 3, 5
+    ids = _rand_ids(rng, T, K, E + 1)
+    mask = rng.random((T, K)) < 0.6
+    si, rm, tpe, off = O.permute_routing(ids, E, 1, active_mask=mask)
+    # brute force: a masked slot is treated like a slot of a non-dispatched id
+    hidden = ids.copy()
+    hidden[~mask] = -1
+    flat = [int(v) for v in hidden.reshape(-1)]
+    counts = [sum(1 for v in flat if v == e) for e in range(E)]
+    assert tpe.tolist() == counts
+    for f, v in enumerate(flat):
+        if 0 <= v < E:
+            assert rm[f] == off[v] + sum(1 for g in range(f) if flat[g] == v)
+        else:
+            assert rm[f] == -1
+    tok_mask = rng.random(T) < 0.5
+    a = O.permute_routing(ids, E, 1, active_mask=tok_mask)
+    b = O.permute_routing(ids, E, 1, active_mask=np.repeat(tok_mask[:, None], K, axis=1))
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_masked_combine_equals_zero_scale():
+    """A slot masked off contributes what a slot of scale 0 contributes."""
+    rng = np.random.default_rng(22)
+    T, K, E, H = 6, 3, 4, 8
+    ids = _rand_ids(rng, T, K, E + 3)
+    si, rm, _, _ = O.permute_routing(ids, E, 3)
+    Y = rng.standard_normal((len(si), H))
+    s = rng.random((T, K))
+    ori, sh = rng.standard_normal((T, H)), rng.standard_normal((T, H))
+    a1, a2, v = rng.random((1, H)), rng.random((1, H)), rng.standard_normal((1, H))
+    mask = rng.random((T, K)) < 0.5
+    got = O.combine(Y, rm, ids, s, sh, ori, E, 1, 1, 1, a1, a2, v, "f64", active_mask=mask)
+    want = O.combine(Y, rm, ids, np.where(mask, s, 0.0), sh, ori, E, 1, 1, 1, a1, a2, v, "f64")
+    assert np.allclose(got, want, atol=1e-14)

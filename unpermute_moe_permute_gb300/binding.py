@@ -55,6 +55,10 @@ _SIGNATURES = {
     "moe_check_status": ([_P, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _SZ),
     "moe_permute": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "moe_permute_masked": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ,
+                            _P, _P], _I),
+    "moe_combine_masked": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                            _P, _P, _P, _P, _P, _P], _I),
     "moe_invert_sorted_indices": ([_P, _I, _I, _P, _P], _I),
     "moe_permute_static_scratch": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P],
                                    _I),
@@ -67,6 +71,7 @@ _SIGNATURES = {
     "moe_combine": ([_P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
                      _P, _P, _P], _I),
     "moe_permute_indices": ([_P, _I, _I, _P, _I, _P, _P, _P, _P], _I),
+    "moe_permute_indices_window": ([_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P], _I),
     "moe_expert_mlp_grad": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                              _P, _P, _P, _P], _I),
     "moe_down_dgrad_swiglu": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -164,6 +169,14 @@ class PermuteResult(NamedTuple):
     expert_offsets: torch.Tensor          # [E+1] int32
 
 
+def _mask(m: torch.Tensor, T: int, K: int) -> torch.Tensor:
+    if m.dtype not in (torch.bool, torch.uint8):
+        raise ValueError("active_mask must be bool or uint8")
+    if tuple(m.shape) not in ((T,), (T, K)):
+        raise ValueError("active_mask must be [T] or [T, K]")
+    return m
+
+
 def moe_permute_workspace_size(T: int, K: int, E: int) -> int:
     return int(load_library().moe_permute_workspace_size(T, K, E))
 
@@ -171,7 +184,9 @@ def moe_permute_workspace_size(T: int, K: int, E: int) -> int:
 def moe_permute(tokens: Optional[torch.Tensor], expert_ids: torch.Tensor, num_experts: int,
                 num_special: int = 0, *, permuted=None, sorted_indices=None, row_map=None,
                 tokens_per_expert=None, expert_offsets=None, workspace=None,
-                dev_status=None) -> PermuteResult:
+                dev_status=None, active_mask=None) -> PermuteResult:
+    """active_mask: optional bool/uint8 [T] (per token) or [T, K] (per slot);
+    masked-off slots are not dispatched."""
     _check(expert_ids, torch.int32, "expert_ids")
     T, K = expert_ids.shape
     dev = expert_ids.device
@@ -191,10 +206,17 @@ def moe_permute(tokens: Optional[torch.Tensor], expert_ids: torch.Tensor, num_ex
     ws = moe_permute_workspace_size(T, K, num_experts)
     if workspace is None:
         workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-    _call("moe_permute", _ptr(tokens), dt, _ptr(expert_ids), T, max(H, 1), K, num_experts,
-          num_special, _ptr(permuted), _ptr(sorted_indices), _ptr(row_map),
-          _ptr(tokens_per_expert), _ptr(expert_offsets), _ptr(workspace),
-          workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream())
+    if active_mask is None:
+        _call("moe_permute", _ptr(tokens), dt, _ptr(expert_ids), T, max(H, 1), K, num_experts,
+              num_special, _ptr(permuted), _ptr(sorted_indices), _ptr(row_map),
+              _ptr(tokens_per_expert), _ptr(expert_offsets), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream())
+    else:
+        _call("moe_permute_masked", _ptr(tokens), dt, _ptr(expert_ids), T, max(H, 1), K,
+              num_experts, num_special, _ptr(_mask(active_mask, T, K)), active_mask.dim(),
+              _ptr(permuted), _ptr(sorted_indices), _ptr(row_map), _ptr(tokens_per_expert),
+              _ptr(expert_offsets), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream())
     return PermuteResult(permuted, sorted_indices, row_map, tokens_per_expert, expert_offsets)
 
 
@@ -379,15 +401,23 @@ def moe_permute_grad(grad_permuted, row_map, T: int, K: int, *, out=None):
 
 def moe_combine(expanded, row_map, expert_ids, scales, num_experts: int, *, shared_x=None,
                 ori_x=None, zero_num: int = 0, copy_num: int = 0, const_num: int = 0,
-                alpha1=None, alpha2=None, const_v=None, out=None, dev_status=None):
+                alpha1=None, alpha2=None, const_v=None, out=None, dev_status=None,
+                active_mask=None):
     T, K = expert_ids.shape
     N, H = expanded.shape
     if out is None:
         out = torch.empty((T, H), dtype=expanded.dtype, device=expanded.device)
-    _call("moe_combine", _ptr(expanded), _dtype(expanded), _ptr(row_map), _ptr(expert_ids),
-          _ptr(scales), _ptr(shared_x), _ptr(ori_x), T, H, K, N, num_experts, zero_num, copy_num,
-          const_num, _ptr(alpha1), _ptr(alpha2), _ptr(const_v), _ptr(out), _ptr(dev_status),
-          _stream())
+    if active_mask is None:
+        _call("moe_combine", _ptr(expanded), _dtype(expanded), _ptr(row_map), _ptr(expert_ids),
+              _ptr(scales), _ptr(shared_x), _ptr(ori_x), T, H, K, N, num_experts, zero_num,
+              copy_num, const_num, _ptr(alpha1), _ptr(alpha2), _ptr(const_v), _ptr(out),
+              _ptr(dev_status), _stream())
+    else:
+        _call("moe_combine_masked", _ptr(expanded), _dtype(expanded), _ptr(row_map),
+              _ptr(expert_ids), _ptr(scales), _ptr(shared_x), _ptr(ori_x),
+              _ptr(_mask(active_mask, T, K)), active_mask.dim(), T, H, K, N, num_experts,
+              zero_num, copy_num, const_num, _ptr(alpha1), _ptr(alpha2), _ptr(const_v), _ptr(out),
+              _ptr(dev_status), _stream())
     return out
 
 
@@ -405,3 +435,21 @@ def moe_permute_indices(counts, R: int, E: int, capacity: int, *, indices=None,
     _call("moe_permute_indices", _ptr(counts), R, E, _ptr(indices), capacity,
           _ptr(tokens_per_expert), _ptr(total), _ptr(dev_status), _stream())
     return indices, tokens_per_expert, total
+
+
+def moe_permute_indices_window(counts, R: int, E_all: int, col_start: int, col_count: int,
+                               capacity: int, *, indices=None, tokens_per_column=None, total=None,
+                               dev_status=None):
+    """Deredundancy dispatch indices: blocks of the expert window
+    [col_start, col_start + col_count) ordered (expert, source)."""
+    dev = counts.device
+    if indices is None:
+        indices = torch.empty(max(capacity, 1), dtype=torch.int32, device=dev)
+    if tokens_per_column is None:
+        tokens_per_column = torch.empty(max(col_count, 1), dtype=torch.int32, device=dev)
+    if total is None:
+        total = torch.empty(1, dtype=torch.int32, device=dev)
+    _call("moe_permute_indices_window", _ptr(counts), R, E_all, col_start, col_count,
+          _ptr(indices), capacity, _ptr(tokens_per_column), _ptr(total), _ptr(dev_status),
+          _stream())
+    return indices, tokens_per_column, total

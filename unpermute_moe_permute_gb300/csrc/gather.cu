@@ -144,7 +144,8 @@ template <typename T, int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
                const int32_t* __restrict__ ids, const float* __restrict__ scales,
-               const T* __restrict__ shared_x, const T* __restrict__ ori_x, int Tn, int H, int K,
+               const T* __restrict__ shared_x, const T* __restrict__ ori_x,
+               const uint8_t* __restrict__ active_mask, int mask_dims, int Tn, int H, int K,
                int N, int E, int zero_num, int copy_num, int const_num, const T* __restrict__ alpha1,
                const T* __restrict__ alpha2, const T* __restrict__ const_v, T* __restrict__ out,
                int32_t* status) {
@@ -174,6 +175,11 @@ combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
       my_arg = (int)(id - klo);
     }
     if (my_kind == kBad) set_status(status, MOE_ERR_BAD_ID);
+    // a slot masked off takes no part: it adds nothing, like a zero expert
+    if (active_mask != nullptr && my_kind != kBad) {
+      const uint8_t a = mask_dims == 1 ? active_mask[t] : active_mask[(size_t)t * K + lane];
+      if (a == 0) my_kind = kZero;
+    }
   }
   int kind[KMAX], arg[KMAX];
   float sc[KMAX];
@@ -248,12 +254,13 @@ void launch_unpermute_grad(const void* g, const void* X, const int32_t* rm, cons
 
 template <typename T, int KMAX>
 void launch_combine(const void* Y, const int32_t* rm, const int32_t* ids, const float* sc,
-                    const void* sh, const void* ori, int Tn, int H, int K, int N, int E, int Z,
-                    int C, int Cn, const void* a1, const void* a2, const void* cv, void* out,
-                    int32_t* st, cudaStream_t s) {
+                    const void* sh, const void* ori, const uint8_t* mask, int mask_dims, int Tn,
+                    int H, int K, int N, int E, int Z, int C, int Cn, const void* a1,
+                    const void* a2, const void* cv, void* out, int32_t* st, cudaStream_t s) {
   combine_kernel<T, KMAX><<<(Tn + kWarpsPerBlock - 1) / kWarpsPerBlock, 256, 0, s>>>(
       static_cast<const T*>(Y), rm, ids, sc, static_cast<const T*>(sh),
-      static_cast<const T*>(ori), Tn, H, K, N, E, Z, C, Cn, static_cast<const T*>(a1),
+      static_cast<const T*>(ori), mask, mask_dims, Tn, H, K, N, E, Z, C, Cn,
+      static_cast<const T*>(a1),
       static_cast<const T*>(a2), static_cast<const T*>(cv), static_cast<T*>(out), st);
   count_launches(1);
 }
@@ -324,12 +331,14 @@ extern "C" int moe_unpermute_grad(const void* grad_out, const void* permuted_tok
   return MOE_OK;
 }
 
-extern "C" int moe_combine(const void* expanded, int dtype, const int32_t* row_map,
-                           const int32_t* expert_ids, const float* scales, const void* shared_x,
-                           const void* ori_x, int T, int H, int K, int N, int E, int zero_num,
-                           int copy_num, int const_num, const void* alpha1, const void* alpha2,
-                           const void* const_v, void* out, int32_t* dev_status,
-                           cudaStream_t stream) {
+extern "C" int moe_combine_masked(const void* expanded, int dtype, const int32_t* row_map,
+                                  const int32_t* expert_ids, const float* scales,
+                                  const void* shared_x, const void* ori_x,
+                                  const uint8_t* active_mask, int mask_dims, int T, int H, int K,
+                                  int N, int E, int zero_num, int copy_num, int const_num,
+                                  const void* alpha1, const void* alpha2, const void* const_v,
+                                  void* out, int32_t* dev_status, cudaStream_t stream) {
+  if (active_mask != nullptr && mask_dims != 1 && mask_dims != 2) return MOE_ERR_INVALID_ARG;
   int rc = check_rows(dtype, T, H, K, N);
   if (rc) return rc;
   if (E <= 0 || zero_num < 0 || copy_num < 0 || const_num < 0) return MOE_ERR_INVALID_ARG;
@@ -345,12 +354,23 @@ extern "C" int moe_combine(const void* expanded, int dtype, const int32_t* row_m
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (dtype == MOE_BF16)
     MOE_DISPATCH_K(K, launch_combine, __nv_bfloat16, expanded, row_map, expert_ids, scales,
-                   shared_x, ori_x, T, H, K, N, E, zero_num, copy_num, const_num, alpha1, alpha2,
-                   const_v, out, dev_status, stream);
+                   shared_x, ori_x, active_mask, mask_dims, T, H, K, N, E, zero_num, copy_num,
+                   const_num, alpha1, alpha2, const_v, out, dev_status, stream);
   else
     MOE_DISPATCH_K(K, launch_combine, float, expanded, row_map, expert_ids, scales, shared_x,
-                   ori_x, T, H, K, N, E, zero_num, copy_num, const_num, alpha1, alpha2, const_v,
-                   out, dev_status, stream);
+                   ori_x, active_mask, mask_dims, T, H, K, N, E, zero_num, copy_num, const_num,
+                   alpha1, alpha2, const_v, out, dev_status, stream);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+extern "C" int moe_combine(const void* expanded, int dtype, const int32_t* row_map,
+                           const int32_t* expert_ids, const float* scales, const void* shared_x,
+                           const void* ori_x, int T, int H, int K, int N, int E, int zero_num,
+                           int copy_num, int const_num, const void* alpha1, const void* alpha2,
+                           const void* const_v, void* out, int32_t* dev_status,
+                           cudaStream_t stream) {
+  return moe_combine_masked(expanded, dtype, row_map, expert_ids, scales, shared_x, ori_x,
+                            nullptr, 0, T, H, K, N, E, zero_num, copy_num, const_num, alpha1,
+                            alpha2, const_v, out, dev_status, stream);
 }

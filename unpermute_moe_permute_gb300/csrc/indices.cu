@@ -1,5 +1,7 @@
 // Rank-major -> expert-major permute indices (hyper_parallel
-// expert_parallel.py, _generate_permute_indices).
+// expert_parallel.py, _generate_permute_indices) and the deredundancy
+// dispatch indices of the same page (_generate_deredundency_dispatch_indices),
+// which are the same construction restricted to a window of expert columns.
 //
 // counts[r*E + e] rows arrived from rank r for local expert e, stored
 // rank-major: [r0.e0 | r0.e1 | ... | r1.e0 | ...].  The expert-major buffer
@@ -57,39 +59,44 @@ __device__ void cta_exclusive_scan(int32_t* a, int n, int32_t* tmp /* >= 32 */,
   __syncthreads();
 }
 
+// counts: [R, E_all] row-major (source r, column e).  The source buffer holds
+// the blocks in that row-major order; the output visits the blocks of the
+// column window [c0, c0 + C) column-major: (c0, r=0..R-1), (c0+1, ...), ...
 __global__ void __launch_bounds__(kIdxThreads)
-permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t* __restrict__ indices,
-                       int capacity, int32_t* __restrict__ tokens_per_expert, int32_t* total,
-                       int32_t* status) {
-  __shared__ int32_t cnt_em[kMaxBlocks];  // counts in (e, r) order
-  __shared__ int32_t src_rm[kMaxBlocks];  // rank-major source starts, (r, e) order
-  __shared__ int32_t dst_em[kMaxBlocks];  // expert-major destination starts, (e, r) order
+permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E_all, int c0, int C,
+                       int32_t* __restrict__ indices, int capacity,
+                       int32_t* __restrict__ tokens_per_column, int32_t* total, int32_t* status) {
+  __shared__ int32_t src_rm[kMaxBlocks];  // source starts, (r, e) order over all columns
+  __shared__ int32_t cnt_w[kMaxBlocks];   // window counts in (c, r) order
+  __shared__ int32_t dst_w[kMaxBlocks];   // destination starts, (c, r) order
   __shared__ int32_t tmp[32];
   __shared__ int32_t s_total;
   __shared__ int32_t s_bad;
-  const int nb = R * E;
+  const int nb = R * E_all, nw = R * C;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   for (int b = threadIdx.x; b < nb; b += kIdxThreads) {
-    const int r = b / E, e = b - r * E;
     int c = counts[b];
     if (c < 0) {
       s_bad = 1;
       c = 0;
     }
     src_rm[b] = c;
-    cnt_em[e * R + r] = c;
-    dst_em[e * R + r] = c;
+    const int r = b / E_all, e = b - r * E_all;
+    if (e >= c0 && e < c0 + C) {
+      cnt_w[(e - c0) * R + r] = c;
+      dst_w[(e - c0) * R + r] = c;
+    }
   }
   __syncthreads();
   cta_exclusive_scan(src_rm, nb, tmp, nullptr);
-  cta_exclusive_scan(dst_em, nb, tmp, &s_total);
+  cta_exclusive_scan(dst_w, nw, tmp, &s_total);
   const int tot = s_total;
   if (blockIdx.x == 0) {
-    for (int e = threadIdx.x; e < E; e += kIdxThreads) {
+    for (int c = threadIdx.x; c < C; c += kIdxThreads) {
       int s = 0;
-      for (int r = 0; r < R; ++r) s += cnt_em[e * R + r];
-      tokens_per_expert[e] = s;
+      for (int r = 0; r < R; ++r) s += cnt_w[c * R + r];
+      tokens_per_column[c] = s;
     }
     if (threadIdx.x == 0) {
       *total = tot;
@@ -100,12 +107,12 @@ permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t
   if (tot > capacity) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = kIdxThreads / 32;
-  for (int b = blockIdx.x * nwarps + warp; b < nb; b += gridDim.x * nwarps) {
-    const int e = b / R, r = b - e * R;  // expert-major block (e, r)
-    const int c = cnt_em[b];
-    const int src = src_rm[r * E + e];
-    const int dst = dst_em[b];
-    for (int j = lane; j < c; j += 32) indices[dst + j] = src + j;
+  for (int b = blockIdx.x * nwarps + warp; b < nw; b += gridDim.x * nwarps) {
+    const int c = b / R, r = b - c * R;
+    const int cnt = cnt_w[b];
+    const int src = src_rm[r * E_all + c0 + c];
+    const int dst = dst_w[b];
+    for (int j = lane; j < cnt; j += 32) indices[dst + j] = src + j;
   }
 }
 
@@ -114,21 +121,32 @@ permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t
 
 using namespace moe;
 
+extern "C" int moe_permute_indices_window(const int32_t* counts, int R, int E_all, int col_start,
+                                          int col_count, int32_t* indices, int capacity,
+                                          int32_t* tokens_per_column, int32_t* total,
+                                          int32_t* dev_status, cudaStream_t stream) {
+  if (R <= 0 || E_all <= 0 || col_start < 0 || col_count < 0 || capacity < 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)col_start + col_count > E_all) return MOE_ERR_SHAPE;
+  if ((long long)R * E_all > kMaxBlocks) return MOE_ERR_SHAPE;
+  if (!counts || !total || (col_count > 0 && !tokens_per_column) || (capacity > 0 && !indices))
+    return MOE_ERR_INVALID_ARG;
+  // Enough CTAs that each warp writes about one block; at most one wave.
+  const int nw = R * col_count;
+  int grid = (nw + 31) / 32;
+  grid = max(1, min(grid, sm_count()));
+  permute_indices_kernel<<<grid, kIdxThreads, 0, stream>>>(counts, R, E_all, col_start, col_count,
+                                                           indices, capacity, tokens_per_column,
+                                                           total, dev_status);
+  count_launches(1);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
 extern "C" int moe_permute_indices(const int32_t* counts, int R, int E, int32_t* indices,
                                    int capacity, int32_t* tokens_per_expert, int32_t* total,
                                    int32_t* dev_status, cudaStream_t stream) {
   if (R <= 0 || E <= 0 || capacity < 0) return MOE_ERR_INVALID_ARG;
-  if ((long long)R * E > kMaxBlocks) return MOE_ERR_SHAPE;
-  if (!counts || !tokens_per_expert || !total || (capacity > 0 && !indices))
-    return MOE_ERR_INVALID_ARG;
-  // Enough CTAs that each warp writes about one (e, r) block; at most one
-  // wave of the GPU.
-  const int nb = R * E;
-  int grid = (nb + 31) / 32;
-  grid = max(1, min(grid, sm_count()));
-  permute_indices_kernel<<<grid, kIdxThreads, 0, stream>>>(counts, R, E, indices, capacity,
-                                                           tokens_per_expert, total, dev_status);
-  count_launches(1);
-  MOE_LAUNCH_CHECK();
-  return MOE_OK;
+  return moe_permute_indices_window(counts, R, E, 0, E, indices, capacity, tokens_per_expert,
+                                    total, dev_status, stream);
 }

@@ -24,21 +24,34 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kSlotsPerWarp = 64;
 constexpr int kChunk = kRouteWarps * kSlotsPerWarp;  // slots per block
 
+// Optional activity mask (the x_active_mask of the torch_npu
+// npu_moe_distribute_combine_v2 parameters): mask_dims 1 = one byte per token
+// [T], 2 = one byte per slot [T, K]; zero = not participating.
+struct SlotMask {
+  const uint8_t* mask;
+  int dims;
+  __device__ __forceinline__ bool active(int f, int K) const {
+    if (mask == nullptr) return true;
+    return (dims == 1 ? mask[f / K] : mask[f]) != 0;
+  }
+};
+
 // Expert a slot is dispatched to, or -1: ids outside [0, E_total) and ids
 // repeated earlier in the same row are not dispatched (and are errors);
-// special ids in [E, E_total) are legal but not dispatched.
+// special ids in [E, E_total) and masked-off slots are legal but not
+// dispatched.
 __device__ __forceinline__ int slot_expert(const int32_t* __restrict__ ids, int f, int K, int E,
-                                           int E_total, bool* bad) {
+                                           int E_total, SlotMask m, bool* bad) {
   const int id = ids[f];
   const int row0 = (f / K) * K;
   bool ok = (id >= 0) && (id < E_total);
   for (int j = row0; j < f; ++j) ok = ok && (ids[j] != id);
   *bad = !ok;
-  return (ok && id < E) ? id : -1;
+  return (ok && id < E && m.active(f, K)) ? id : -1;
 }
 
 __global__ void __launch_bounds__(kRouteThreads)
-route_hist_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total,
+route_hist_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total, SlotMask m,
                   int32_t* __restrict__ blk_counts, int32_t* status) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += kRouteThreads) hist[e] = 0;
@@ -48,7 +61,7 @@ route_hist_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_t
   bool any_bad = false;
   for (int f = base + threadIdx.x; f < end; f += kRouteThreads) {
     bool bad;
-    const int e = slot_expert(ids, f, K, E, E_total, &bad);
+    const int e = slot_expert(ids, f, K, E, E_total, m, &bad);
     any_bad |= bad;
     if (e >= 0) atomicAdd(&hist[e], 1);
   }
@@ -124,7 +137,7 @@ route_scan_kernel(int32_t* __restrict__ blk, int nblk, int E, int32_t* __restric
 }
 
 __global__ void __launch_bounds__(kRouteThreads)
-route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total,
+route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total, SlotMask m,
                      const int32_t* __restrict__ blk_base, int32_t* __restrict__ sorted_indices,
                      int32_t* __restrict__ row_map) {
   extern __shared__ int32_t cnt[];  // [kRouteWarps][E]
@@ -142,7 +155,7 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int 
     ex[i] = -1;
     if (f < TK) {
       bool bad;
-      ex[i] = slot_expert(ids, f, K, E, E_total, &bad);
+      ex[i] = slot_expert(ids, f, K, E, E_total, m, &bad);
       if (ex[i] >= 0) atomicAdd(&my[ex[i]], 1);
     }
   }
@@ -243,11 +256,13 @@ extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
   return (size_t)((nblk > 0 ? nblk : 1) * E * sizeof(int32_t));
 }
 
-extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T, int H,
-                           int K, int E, int num_special, void* permuted, int32_t* sorted_indices,
-                           int32_t* row_map, int32_t* tokens_per_expert, int32_t* expert_offsets,
-                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           cudaStream_t stream) {
+extern "C" int moe_permute_masked(const void* tokens, int dtype, const int32_t* expert_ids, int T,
+                                  int H, int K, int E, int num_special, const uint8_t* active_mask,
+                                  int mask_dims, void* permuted, int32_t* sorted_indices,
+                                  int32_t* row_map, int32_t* tokens_per_expert,
+                                  int32_t* expert_offsets, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, cudaStream_t stream) {
+  if (active_mask != nullptr && mask_dims != 1 && mask_dims != 2) return MOE_ERR_INVALID_ARG;
   if (T < 0 || H <= 0 || K <= 0 || E <= 0 || num_special < 0) return MOE_ERR_INVALID_ARG;
   if (K > kMaxK || E > kMaxExperts || (long long)K > (long long)E + num_special)
     return MOE_ERR_SHAPE;
@@ -276,15 +291,16 @@ extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_
   }
   int32_t* blk = static_cast<int32_t*>(workspace);
   const int E_total = E + num_special;
+  const SlotMask m{active_mask, mask_dims};
   route_hist_kernel<<<nblk, kRouteThreads, E * sizeof(int32_t), stream>>>(expert_ids, TK, K, E,
-                                                                         E_total, blk, dev_status);
+                                                                         E_total, m, blk, dev_status);
   route_scan_kernel<<<1, 1024, 0, stream>>>(blk, nblk, E, tokens_per_expert, expert_offsets);
   const size_t scatter_smem = (size_t)kRouteWarps * E * sizeof(int32_t);
   if (scatter_smem > 48 * 1024)
     cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)scatter_smem);
-  route_scatter_kernel<<<nblk, kRouteThreads, scatter_smem, stream>>>(expert_ids, TK, K, E, E_total,
-                                                                      blk, sorted_indices, row_map);
+  route_scatter_kernel<<<nblk, kRouteThreads, scatter_smem, stream>>>(
+      expert_ids, TK, K, E, E_total, m, blk, sorted_indices, row_map);
   count_launches(3);
   if (tokens != nullptr && T > 0) {
     const int row_bytes = H * dtype_size(dtype);
@@ -295,6 +311,16 @@ extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_
   }
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T, int H,
+                           int K, int E, int num_special, void* permuted, int32_t* sorted_indices,
+                           int32_t* row_map, int32_t* tokens_per_expert, int32_t* expert_offsets,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           cudaStream_t stream) {
+  return moe_permute_masked(tokens, dtype, expert_ids, T, H, K, E, num_special, nullptr, 0,
+                            permuted, sorted_indices, row_map, tokens_per_expert, expert_offsets,
+                            workspace, workspace_bytes, dev_status, stream);
 }
 
 extern "C" int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, int TK,
