@@ -39,19 +39,19 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
+constexpr int BM = 128, BN = 256, UK = 16;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half of the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;        // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;   // one 64 (M/N) x 64 (K) box, 8 KB
 constexpr uint32_t TMEM_COLS = 512;
 // Epilogue staging: each epilogue warp owns a ring of NBUF units of 32 rows x
 // 32 bf16 (2 KB, 64-byte swizzle) that TMA stores copy to global memory.
 constexpr uint32_t UNIT_BYTES = 32 * 64;
-constexpr uint32_t CTRL_BYTES = 128 + (kMaxExperts + 1) * 4 + 32 * 4;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
+// control block: 2 * stages + 5 mbarriers, then the TMEM address, the abort
+// flag, the tile prefix and its scan scratch
+constexpr uint32_t kHolderOff = 8 * (2 * kMaxStages + 5);
+constexpr uint32_t kPrefixOff = kHolderOff + 24;
+constexpr uint32_t CTRL_BYTES = kPrefixOff + (kMaxExperts + 1) * 4 + 32 * 4;
 
 enum Kind : int {
   kFwdGateUp = 0,
@@ -69,10 +69,19 @@ struct Traits {
   static constexpr bool wgrad = (KIND == kWgradDown || KIND == kWgradGateUp);
   static constexpr int n_per_tile = (KIND == kFwdGateUp) ? 128 : 256;  // output columns
   static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
-  // Every kind is fed through the load pipeline (measured: a fourth stage
-  // beats a second staging unit per epilogue warp for all six).
+  // k-block depth and ring depth: 64-deep blocks (one 128-byte swizzle row)
+  // in 4 stages for every kind.  Measured on GB300: a fourth stage beats a
+  // second staging unit per epilogue warp, and for the wgrads 32-deep blocks
+  // in 8 stages (a ring holding two tiles) lose more to the smaller TMA
+  // boxes than they gain from overlap.
+  static constexpr int bk = 64;
   static constexpr int stages = 4;
   static constexpr int nbuf = 1;
+  static constexpr uint32_t a_bytes = BM * bk * 2;
+  static constexpr uint32_t b_bytes = BN * bk * 2;
+  static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
+  static constexpr uint32_t mn_box = 64 * bk * 2;  // one 64 (M/N) x bk (K) MN-major box
+  static_assert(stages <= kMaxStages, "more stages than the control block holds");
   // Cluster size.  With cs = 2, CTA pairs take vertically adjacent 128-row
   // tiles that share their B tile: each CTA loads half of B and multicasts
   // it to both (32 KB instead of 48 KB from L2 per CTA and k block).  On
@@ -81,8 +90,7 @@ struct Traits {
   // single CTAs are used.
   static constexpr int cs = 1;
   static constexpr uint32_t staging_bytes = kEpiWarps * nbuf * UNIT_BYTES;
-  static constexpr uint32_t smem_bytes = stages * STAGE_BYTES + staging_bytes + CTRL_BYTES + 1024;
-  static_assert(8 * (2 * stages + 5) <= 104, "barriers overlap the control words");
+  static constexpr uint32_t smem_bytes = stages * stage_bytes + staging_bytes + CTRL_BYTES + 1024;
   static_assert(smem_bytes <= 232448, "more shared memory than one CTA may use");
 };
 
@@ -127,7 +135,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.hi = r.hi;
     x.m0 = r.lo + (mg - prefix[e]) * (BM * CS) + rank * BM;
     x.n0 = nt * Traits<KIND>::n_per_tile;
-    x.kblocks = p.Kd / BK;
+    x.kblocks = p.Kd / Traits<KIND>::bk;
   } else {
     const int m_groups = (p.m_tiles + CS - 1) / CS;
     const int per = m_groups * p.n_tiles;
@@ -139,7 +147,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.hi = r.hi;
     x.m0 = (mg * CS + rank) * BM;
     x.n0 = nt * BN;
-    x.kblocks = (r.hi - r.lo + BK - 1) / BK;
+    x.kblocks = (r.hi - r.lo + Traits<KIND>::bk - 1) / Traits<KIND>::bk;
   }
   return x;
 }
@@ -155,7 +163,9 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
                                            int rank) {
   constexpr int CS = Traits<KIND>::cs;
   constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
-  const int k0 = kb * BK;
+  constexpr uint32_t B_BYTES = Traits<KIND>::b_bytes;
+  constexpr uint32_t MN_BOX_BYTES = Traits<KIND>::mn_box;
+  const int k0 = kb * Traits<KIND>::bk;
   auto b3 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by, int bz) {
     if constexpr (CS > 1) tma_load_3d_mc(dst, m, bar, bx, by, bz, kMask);
     else tma_load_3d(dst, m, bar, bx, by, bz);
@@ -464,6 +474,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   constexpr int STAGES = Traits<KIND>::stages;
   constexpr int NBUF = Traits<KIND>::nbuf;
   constexpr int CS = Traits<KIND>::cs;
+  constexpr int BK = Traits<KIND>::bk;
+  constexpr uint32_t A_BYTES = Traits<KIND>::a_bytes;
+  constexpr uint32_t B_BYTES = Traits<KIND>::b_bytes;
+  constexpr uint32_t STAGE_BYTES = Traits<KIND>::stage_bytes;
+  constexpr uint32_t MN_BOX_BYTES = Traits<KIND>::mn_box;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -478,9 +493,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   auto tfull_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = ctrl + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gctrl + 104);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 108);
-  int32_t* prefix = reinterpret_cast<int32_t*>(gctrl + 128);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gctrl + kHolderOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + kHolderOff + 4);
+  int32_t* prefix = reinterpret_cast<int32_t*>(gctrl + kPrefixOff);
   int32_t* scratch = prefix + (kMaxExperts + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -585,13 +600,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             nk = (rem + UK - 1) / UK;
             const int z0 = rem, z1 = nk * UK, zl = z1 - z0;
             if (zl > 0) {
-              const int n16 = zl * 6 * 8;  // lines x boxes x 16-byte chunks
-              for (int i = lane; i < n16; i += 32) {
-                const int chunk = i & 7, line = i >> 3;
-                const int box = line / zl, r = z0 + line % zl;
-                const uint32_t addr = (box < 2 ? sa + box * MN_BOX_BYTES : sb + (box - 2) * MN_BOX_BYTES) +
-                                      r * 128 + chunk * 16;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+              // lane i zeroes 16-byte chunk (i & 7) of tail row z0 + (i >> 3)
+              // in all six operand boxes (2 of A, 4 of B)
+              for (int i = lane; i < zl * 8; i += 32) {
+                const uint32_t off = (uint32_t)(z0 + (i >> 3)) * 128u + (uint32_t)(i & 7) * 16u;
+#pragma unroll
+                for (int box = 0; box < 2; ++box) st_shared_v4(sa + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int box = 0; box < 4; ++box) st_shared_v4(sb + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
               }
               fence_proxy_async_smem();
             }
@@ -863,7 +879,7 @@ int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H,
 int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, int N, int H,
                            int I, int E, void* dWd, int32_t* status, cudaStream_t s) {
   if (int rc = device_ok()) return rc;
-  const uint32_t box_mn2[2] = {64, 64};
+  const uint32_t box_mn2[2] = {64, (uint32_t)Traits<kWgradDown>::bk};
   CUtensorMap m_a, m_b;
   const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
   const uint64_t d_a[2] = {(uint64_t)H, rows};
@@ -887,7 +903,7 @@ int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off
                               int I, int E, void* dWg, void* dWu, int32_t* status,
                               cudaStream_t s) {
   if (int rc = device_ok()) return rc;
-  const uint32_t box_mn2[2] = {64, 64};
+  const uint32_t box_mn2[2] = {64, (uint32_t)Traits<kWgradGateUp>::bk};
   CUtensorMap m_a, m_b;
   const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
   const uint64_t d_a[2] = {(uint64_t)2 * I, rows};
