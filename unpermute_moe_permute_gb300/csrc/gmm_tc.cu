@@ -75,8 +75,10 @@ struct Traits {
   // in 8 stages (a ring holding two tiles) lose more to the smaller TMA
   // boxes than they gain from overlap.
   static constexpr int bk = 64;
-  static constexpr int stages = 4;
-  static constexpr int nbuf = 1;
+  // The SwiGLU-backward epilogue stages two units (dg, du) per piece and is
+  // the slower side of its kernel: it trades a stage for a two-unit ring.
+  static constexpr int stages = KIND == kDgradDown ? 3 : 4;
+  static constexpr int nbuf = KIND == kDgradDown ? 2 : 1;
   static constexpr uint32_t a_bytes = BM * bk * 2;
   static constexpr uint32_t b_bytes = BN * bk * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
