@@ -39,7 +39,7 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, UK = 16;
+constexpr int BM = 128, UK = 16;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half of the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t TMEM_COLS = 512;
@@ -67,8 +67,13 @@ struct Traits {
   static constexpr bool a_mn = (KIND == kWgradDown || KIND == kWgradGateUp);
   static constexpr bool b_mn = (KIND >= kDgradDown);
   static constexpr bool wgrad = (KIND == kWgradDown || KIND == kWgradGateUp);
-  static constexpr int n_per_tile = (KIND == kFwdGateUp) ? 128 : 256;  // output columns
-  static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
+  // UMMA N (256 for every kind; a 192-wide down-dgrad tile, which evens out
+  // its waves at I = 768, measured slower because that kernel is bound by
+  // its epilogue, not by idle SMs).
+  static constexpr int bn = 256;
+  static constexpr int pieces = bn / 32;  // 32-column epilogue pieces per tile
+  static constexpr int n_per_tile = (KIND == kFwdGateUp) ? bn / 2 : bn;  // output columns
+  static constexpr uint32_t idesc = idesc_bf16_f32(BM, bn, a_mn, b_mn);
   // k-block depth and ring depth: 64-deep blocks (one 128-byte swizzle row)
   // in 4 stages for every kind.  Measured on GB300: a fourth stage beats a
   // second staging unit per epilogue warp, and for the wgrads 32-deep blocks
@@ -80,7 +85,7 @@ struct Traits {
   static constexpr int stages = KIND == kDgradDown ? 3 : 4;
   static constexpr int nbuf = KIND == kDgradDown ? 2 : 1;
   static constexpr uint32_t a_bytes = BM * bk * 2;
-  static constexpr uint32_t b_bytes = BN * bk * 2;
+  static constexpr uint32_t b_bytes = bn * bk * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
   static constexpr uint32_t mn_box = 64 * bk * 2;  // one 64 (M/N) x bk (K) MN-major box
   static_assert(stages <= kMaxStages, "more stages than the control block holds");
@@ -148,7 +153,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.lo = r.lo;
     x.hi = r.hi;
     x.m0 = (mg * CS + rank) * BM;
-    x.n0 = nt * BN;
+    x.n0 = nt * Traits<KIND>::bn;
     x.kblocks = (r.hi - r.lo + Traits<KIND>::bk - 1) / Traits<KIND>::bk;
   }
   return x;
@@ -177,7 +182,7 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
     else tma_load_2d(dst, m, bar, bx, by);
   };
   // which of the B boxes this CTA loads: K-major B has 2, MN-major B has 4
-  constexpr int kBoxes = Traits<KIND>::b_mn ? 4 : 2;
+  constexpr int kBoxes = Traits<KIND>::b_mn ? Traits<KIND>::bn / 64 : Traits<KIND>::bn / 128;
   constexpr int kMine = kBoxes / CS;
   const int j0 = rank * kMine;
   if constexpr (KIND == kFwdGateUp) {
@@ -349,8 +354,9 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
         }
       }
     } else if constexpr (KIND == kFwdDown || KIND == kDgradGateUp) {
+      constexpr int HP = Traits<KIND>::pieces / 2;
 #pragma unroll 1
-      for (int c = 4 * half; c < 4 * half + 4; ++c) {
+      for (int c = HP * half; c < HP * half + HP; ++c) {
         const int col = x.n0 + c * 32;
         if (col >= p.Nout) break;
         uint32_t v[32], w[16];
@@ -382,13 +388,14 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
           for (int q = 0; q < 4; ++q) a[q] = b[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       };
-      fetch(x.n0 + half * 128, rg, ru);
+      constexpr int HP = Traits<KIND>::pieces / 2;
+      fetch(x.n0 + half * HP * 32, rg, ru);
 #pragma unroll 1
-      for (int c = 4 * half; c < 4 * half + 4; ++c) {
+      for (int c = HP * half; c < HP * half + HP; ++c) {
         const int col = x.n0 + c * 32;
         if (col >= I) break;
         uint4 ng[4], nu[4];
-        fetch(c + 1 < 4 * half + 4 ? col + 32 : I, ng, nu);
+        fetch(c + 1 < HP * half + HP ? col + 32 : I, ng, nu);
         uint32_t v[32];
         tmem_ld_32x32b_x32(tacc + c * 32, v);
         tmem_ld_wait();
@@ -447,8 +454,9 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
       }
     }
     const bool empty = x.kblocks == 0;  // uniform over the tile
+    constexpr int HP = Traits<KIND>::pieces / 2;
 #pragma unroll 1
-    for (int c = 4 * half; c < 4 * half + 4; ++c) {
+    for (int c = HP * half; c < HP * half + HP; ++c) {
       const int col = x.n0 + c * 32;
       if (col >= p.Nout) break;
       uint32_t w[16];
@@ -582,7 +590,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       const uint32_t aph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
       tc_fence_after();
-      const uint32_t tacc = tmem_base + acc * BN;
+      const uint32_t tacc = tmem_base + acc * Traits<KIND>::bn;
       for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
         const int s = g % STAGES;
         const uint32_t ph = (g / STAGES) & 1;
@@ -650,7 +658,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       const uint32_t aph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))) break;
       tc_fence_after();
-      const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t tacc = tmem_base + acc * Traits<KIND>::bn + ((uint32_t)(quarter * 32) << 16);
       epilogue<KIND>(x, p, tacc, quarter, half, lane, ring, &mapC0, &mapC1);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
@@ -844,7 +852,7 @@ int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* o
   p.Kd = H;
   p.I = I;
   p.Nout = I;
-  p.n_tiles = (I + 255) / 256;
+  p.n_tiles = (I + Traits<kDgradDown>::bn - 1) / Traits<kDgradDown>::bn;
   p.out = static_cast<__nv_bfloat16*>(dgu);
   p.aux = static_cast<const __nv_bfloat16*>(gate_up);
   CUtensorMap c_dgu;
