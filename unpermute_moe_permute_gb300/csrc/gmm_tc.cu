@@ -41,15 +41,14 @@ namespace tc {
 
 constexpr int BM = 128, UK = 16;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half of the columns
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t TMEM_COLS = 512;
 // Epilogue staging: each epilogue warp owns a ring of NBUF units of 32 rows x
 // 32 bf16 (2 KB, 64-byte swizzle) that TMA stores copy to global memory.
 constexpr uint32_t UNIT_BYTES = 32 * 64;
 constexpr int kMaxStages = 8;
-// control block: 2 * stages + 5 mbarriers, then the TMEM address, the abort
+// control block: 4 * stages + 5 mbarriers, then the TMEM address, the abort
 // flag, the tile prefix and its scan scratch
-constexpr uint32_t kHolderOff = 8 * (2 * kMaxStages + 5);
+constexpr uint32_t kHolderOff = 8 * (4 * kMaxStages + 5);
 constexpr uint32_t kPrefixOff = kHolderOff + 24;
 constexpr uint32_t CTRL_BYTES = kPrefixOff + 2 * (kMaxExperts + 1) * 4 + 32 * 4;
 
@@ -67,6 +66,10 @@ struct Traits {
   static constexpr bool a_mn = (KIND == kWgradDown || KIND == kWgradGateUp);
   static constexpr bool b_mn = (KIND >= kDgradDown);
   static constexpr bool wgrad = (KIND == kWgradDown || KIND == kWgradGateUp);
+  // TMA producer, MMA issuer, epilogue warps, and for the wgrads one warp
+  // that zeroes the rows past an expert's end in its last k block, so that
+  // the MMA-issuing warp only issues.
+  static constexpr int threads = 64 + 32 * kEpiWarps + (wgrad ? 32 : 0);
   // UMMA N (256 for every kind; a 192-wide down-dgrad tile, which evens out
   // its waves at I = 768, measured slower because that kernel is bound by
   // its epilogue, not by idle SMs).
@@ -123,6 +126,26 @@ struct Tile {
   int m0, n0;     // first output row / column of the tile
   int kblocks;    // 64-deep k blocks
 };
+
+// Wgrad k block kb of tile x (k = the expert's token rows): the MMAs cover
+// nk 16-row groups; rows [z0, z0 + zl) of the block lie inside the last of
+// them but belong to the next expert and must read as zero.
+struct KTail {
+  int nk, z0, zl;
+};
+
+template <int KIND>
+__device__ __forceinline__ KTail k_tail(const Tile& x, int kb) {
+  constexpr int BK = Traits<KIND>::bk;
+  const int rem = x.hi - (x.lo + kb * BK);
+  KTail r{BK / UK, BK, 0};
+  if (rem < BK) {
+    r.nk = (rem + UK - 1) / UK;
+    r.z0 = rem;
+    r.zl = r.nk * UK - rem;
+  }
+  return r;
+}
 
 // Cluster tile t: a group of CS vertically adjacent 128-row tiles of one
 // expert and one n tile; this CTA (cluster rank `rank`) takes the rank-th.
@@ -481,7 +504,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Traits<KIND>::threads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
               const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapC0,
               const __grid_constant__ CUtensorMap mapC1, const Params p) {
@@ -507,6 +530,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   auto tfull_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = ctrl + 8u * (2 * STAGES + 4);
+  // wgrad tails: the producer marks a stage whose block has a tail
+  // (tail_bar), the fix warp zeroes it once loaded and releases it (fix_bar)
+  auto fix_bar = [&](int s) { return ctrl + 8u * (2 * STAGES + 5 + s); };
+  auto tail_bar = [&](int s) { return ctrl + 8u * (3 * STAGES + 5 + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gctrl + kHolderOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + kHolderOff + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(gctrl + kPrefixOff);
@@ -524,6 +551,12 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       mbar_init(tempty_bar(a), kEpiWarps * 32);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (Traits<KIND>::wgrad) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(fix_bar(s), 1);
+        mbar_init(tail_bar(s), 1);
+      }
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -581,6 +614,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, full_bar(s), &mapA,
                            &mapB0, &mapB1, rank);
           issued[s] = (int)ph;
+          if constexpr (Traits<KIND>::wgrad)
+            if (k_tail<KIND>(x, kb).zl > 0) mbar_arrive(tail_bar(s));
         }
       }
       // wait for every copy this thread issued before the CTA may exit
@@ -591,6 +626,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     int g = 0, it = 0;
+    uint32_t fixph = 0;  // bit s: parity of the next fix_bar(s) phase
     bool run = true;
     for (int t = t_first; run && t < total; t += t_step, ++it) {
       const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
@@ -610,26 +646,17 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
         int nk = BK / UK;
         if constexpr (Traits<KIND>::wgrad) {
-          // Last k block of an expert: rows past the expert's end belong to
-          // the next expert.  Skip whole 16-row groups past the end and zero
-          // the rest of the last group in every operand box.
-          const int rem = x.hi - (x.lo + kb * BK);
-          if (rem < BK) {
-            nk = (rem + UK - 1) / UK;
-            const int z0 = rem, z1 = nk * UK, zl = z1 - z0;
-            if (zl > 0) {
-              // lane i zeroes 16-byte chunk (i & 7) of tail row z0 + (i >> 3)
-              // in all six operand boxes (2 of A, 4 of B)
-              for (int i = lane; i < zl * 8; i += 32) {
-                const uint32_t off = (uint32_t)(z0 + (i >> 3)) * 128u + (uint32_t)(i & 7) * 16u;
-#pragma unroll
-                for (int box = 0; box < 2; ++box) st_shared_v4(sa + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int box = 0; box < 4; ++box) st_shared_v4(sb + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
-              }
-              fence_proxy_async_smem();
+          // Last k block of an expert: skip whole 16-row groups past its end;
+          // the rest of the last group is zeroed by the fix warp.
+          const KTail kt = k_tail<KIND>(x, kb);
+          nk = kt.nk;
+          if (kt.zl > 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(fix_bar(s), (fixph >> s) & 1u, abort_flag, p.status))) {
+              run = false;
+              break;
             }
-            __syncwarp();
+            fixph ^= 1u << s;
+            tc_fence_after();
           }
         }
         if (lane == 0) {
@@ -654,7 +681,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       mbar_wait(drain_bar, 0, abort_flag, p.status, false);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ---------------- epilogue warps 2..9 ----------------
     const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
@@ -674,6 +701,43 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // the CTA's stores must be complete before it exits
     if (lane == 0) bulk_wait_group_all();
     __syncwarp();
+  } else if constexpr (Traits<KIND>::wgrad) {
+    // ---------------- fix warp 10 (wgrads): zero the tail rows ----------------
+    // Visits the tail blocks in the producer's order.  Stage s is refilled
+    // only after the MMA consumed it, which waits for this warp, so each of
+    // tail_bar(s), full_bar(s) and fix_bar(s) is at most one phase ahead.
+    int g = 0;
+    uint32_t tph = 0;  // bit s: parity of the next tail_bar(s) phase
+    bool run = true;
+    for (int t = t_first; run && t < total; t += t_step) {
+      const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
+      for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
+        const KTail kt = k_tail<KIND>(x, kb);
+        if (kt.zl == 0) continue;
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(tail_bar(s), (tph >> s) & 1u, abort_flag, p.status)) ||
+            !__all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, abort_flag, p.status))) {
+          run = false;
+          break;
+        }
+        tph ^= 1u << s;
+        const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
+        // lane i zeroes 16-byte chunk (i & 7) of tail row z0 + (i >> 3) in
+        // all six operand boxes (2 of A, 4 of B); the rows are 128 bytes and
+        // the 128-byte swizzle only permutes chunks within a row
+        for (int i = lane; i < kt.zl * 8; i += 32) {
+          const uint32_t off = (uint32_t)(kt.z0 + (i >> 3)) * 128u + (uint32_t)(i & 7) * 16u;
+#pragma unroll
+          for (int box = 0; box < 2; ++box) st_shared_v4(sa + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int box = 0; box < 4; ++box) st_shared_v4(sb + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fix_bar(s));
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -736,7 +800,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   if constexpr (CS == 1) {
     // One persistent CTA per SM.  A plain launch: the same kernel launched
     // through the cluster-attribute path (cluster size 1) measured ~20 % slower.
-    gmm_tc_kernel<KIND><<<sm_count(), kThreads, Traits<KIND>::smem_bytes, s>>>(a, b0, b1, c0, c1, p);
+    gmm_tc_kernel<KIND><<<sm_count(), Traits<KIND>::threads, Traits<KIND>::smem_bytes, s>>>(a, b0, b1, c0, c1, p);
     count_launches(1);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
@@ -747,7 +811,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   at[0].val.clusterDim.x = CS;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Traits<KIND>::threads, 1, 1);
   cfg.dynamicSmemBytes = Traits<KIND>::smem_bytes;
   cfg.stream = s;
   cfg.attrs = at;
