@@ -76,7 +76,21 @@ struct Traits {
   static constexpr int bn = 256;
   static constexpr int pieces = bn / 32;  // 32-column epilogue pieces per tile
   static constexpr int n_per_tile = (KIND == kFwdGateUp) ? bn / 2 : bn;  // output columns
-  static constexpr uint32_t idesc = idesc_bf16_f32(BM, bn, a_mn, b_mn);
+  // CTA pairs (cta_group::2): the two CTAs of a cluster take vertically
+  // adjacent 128-row tiles of one expert and n tile and hold half of the
+  // B tile each, so per SM the MMA reads and the TMA writes 32 KB of shared
+  // memory per k block instead of 48 KB.  The price is a wasted half tile
+  // for every expert with an odd number of 128-row tiles.  Measured at
+  // T=4096 H=2048 E=128 K=8 I=768 (same GPU, back to back, us):
+  //   gate_up 204 pair / 207 single, down 107 / 108,
+  //   down dgrad 160 / 150, gate_up dgrad 196 / 195,
+  // so pairs are used for the forward kinds.  The wgrads stay single: their
+  // expert tail rows are zeroed in shared memory after the loads land,
+  // which the leader cannot observe for the peer's loads.
+  static constexpr bool pair = (KIND == kFwdGateUp || KIND == kFwdDown);
+  static constexpr int cs = pair ? 2 : 1;  // CTAs per cluster
+  static constexpr int b_rows = pair ? bn / 2 : bn;  // B rows (N) this CTA holds
+  static constexpr uint32_t idesc = idesc_bf16_f32(BM * cs, bn, a_mn, b_mn);
   // k-block depth and ring depth: 64-deep blocks (one 128-byte swizzle row)
   // in 4 stages for every kind.  Measured on GB300: a fourth stage beats a
   // second staging unit per epilogue warp, and for the wgrads 32-deep blocks
@@ -85,20 +99,14 @@ struct Traits {
   static constexpr int bk = 64;
   // The SwiGLU-backward epilogue stages two units (dg, du) per piece and is
   // the slower side of its kernel: it trades a stage for a two-unit ring.
-  static constexpr int stages = KIND == kDgradDown ? 3 : 4;
   static constexpr int nbuf = KIND == kDgradDown ? 2 : 1;
+  static constexpr int stages = pair ? (KIND == kDgradDown ? 5 : 6) : (KIND == kDgradDown ? 3 : 4);
   static constexpr uint32_t a_bytes = BM * bk * 2;
-  static constexpr uint32_t b_bytes = bn * bk * 2;
+  static constexpr uint32_t b_bytes = b_rows * bk * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
   static constexpr uint32_t mn_box = 64 * bk * 2;  // one 64 (M/N) x bk (K) MN-major box
   static_assert(stages <= kMaxStages, "more stages than the control block holds");
-  // Cluster size.  With cs = 2, CTA pairs take vertically adjacent 128-row
-  // tiles that share their B tile: each CTA loads half of B and multicasts
-  // it to both (32 KB instead of 48 KB from L2 per CTA and k block).  On
-  // GB300 that measured slower for all six kinds at the benchmark shapes
-  // (the pair runs in lockstep and fewer SMs hold whole clusters), so
-  // single CTAs are used.
-  static constexpr int cs = 1;
+  static_assert(!(pair && wgrad), "the wgrad tail fix-up is single-CTA");
   static constexpr uint32_t staging_bytes = kEpiWarps * nbuf * UNIT_BYTES;
   static constexpr uint32_t smem_bytes = stages * stage_bytes + staging_bytes + CTRL_BYTES + 1024;
   static_assert(smem_bytes <= 232448, "more shared memory than one CTA may use");
@@ -182,60 +190,56 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
   return x;
 }
 
-// TMA loads of k block kb of tile x into one stage.  A is this CTA's own.
-// B is shared by the cluster: with CS = 2 this CTA loads half of it (one of
-// the two 128-row K-major boxes, or two of the four 64-column MN-major
-// boxes) and multicasts it into both CTAs.
+// TMA loads of k block kb of tile x into one stage: this CTA's own 128 rows
+// of A (unless load_a is false) and its part of B: all of it for a single
+// CTA, the rank-th half (128 of the 256 N rows) in a pair.  `bar` receives
+// the bytes: this CTA's full barrier, or the leader's in a pair.
 template <int KIND>
 __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& p, uint32_t sa,
                                            uint32_t sb, uint32_t bar, const CUtensorMap* mA,
                                            const CUtensorMap* mB0, const CUtensorMap* mB1,
-                                           int rank) {
-  constexpr int CS = Traits<KIND>::cs;
-  constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
-  constexpr uint32_t B_BYTES = Traits<KIND>::b_bytes;
+                                           int rank, bool load_a) {
+  constexpr bool PAIR = Traits<KIND>::pair;
+  constexpr int B_ROWS = Traits<KIND>::b_rows;
   constexpr uint32_t MN_BOX_BYTES = Traits<KIND>::mn_box;
   const int k0 = kb * Traits<KIND>::bk;
-  auto b3 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by, int bz) {
-    if constexpr (CS > 1) tma_load_3d_mc(dst, m, bar, bx, by, bz, kMask);
-    else tma_load_3d(dst, m, bar, bx, by, bz);
-  };
-  auto b2 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by) {
-    if constexpr (CS > 1) tma_load_2d_mc(dst, m, bar, bx, by, kMask);
+  auto l2 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by) {
+    if constexpr (PAIR) tma_load_2d_pair(dst, m, bar, bx, by);
     else tma_load_2d(dst, m, bar, bx, by);
   };
-  // which of the B boxes this CTA loads: K-major B has 2, MN-major B has 4
-  constexpr int kBoxes = Traits<KIND>::b_mn ? Traits<KIND>::bn / 64 : Traits<KIND>::bn / 128;
-  constexpr int kMine = kBoxes / CS;
-  const int j0 = rank * kMine;
+  auto l3 = [&](uint32_t dst, const CUtensorMap* m, int bx, int by, int bz) {
+    if constexpr (PAIR) tma_load_3d_pair(dst, m, bar, bx, by, bz);
+    else tma_load_3d(dst, m, bar, bx, by, bz);
+  };
+  const int nb = x.n0 + (PAIR ? rank * B_ROWS : 0);  // first B row (N) of this CTA's part
   if constexpr (KIND == kFwdGateUp) {
-    tma_load_2d(sa, mA, bar, k0, x.m0);
-#pragma unroll
-    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * (B_BYTES / 2), j == 0 ? mB0 : mB1, k0, x.n0, x.e);
-  } else if constexpr (KIND == kFwdDown) {
-    tma_load_2d(sa, mA, bar, k0, x.m0);
-    if constexpr (CS == 1) {
-      b3(sb, mB0, k0, x.n0, x.e);  // all 256 rows of the W_down panel in one box
+    // B tile = 128 rows of W_gate, then the same 128 rows of W_up
+    if (load_a) l2(sa, mA, k0, x.m0);
+    if constexpr (PAIR) {
+      l3(sb, rank == 0 ? mB0 : mB1, k0, x.n0, x.e);
     } else {
-#pragma unroll
-      for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * (B_BYTES / 2), mB0, k0, x.n0 + 128 * j, x.e);
+      l3(sb, mB0, k0, x.n0, x.e);
+      l3(sb + Traits<KIND>::b_bytes / 2, mB1, k0, x.n0, x.e);
     }
+  } else if constexpr (KIND == kFwdDown) {
+    if (load_a) l2(sa, mA, k0, x.m0);
+    l3(sb, mB0, k0, nb, x.e);  // B_ROWS rows of the W_down panel in one box
   } else if constexpr (KIND == kDgradDown) {
-    tma_load_2d(sa, mA, bar, k0, x.m0);
+    if (load_a) l2(sa, mA, k0, x.m0);
 #pragma unroll
-    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * MN_BOX_BYTES, mB0, x.n0 + j * 64, k0, x.e);
+    for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, k0, x.e);
   } else if constexpr (KIND == kDgradGateUp) {
-    tma_load_2d(sa, mA, bar, k0, x.m0);
+    if (load_a) l2(sa, mA, k0, x.m0);
     const bool up = k0 >= p.I;
     const int kk = up ? k0 - p.I : k0;
 #pragma unroll
-    for (int j = j0; j < j0 + kMine; ++j) b3(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, x.n0 + j * 64, kk, x.e);
+    for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, nb + j * 64, kk, x.e);
   } else {  // wgrad: both operands MN-major, k = token rows of the expert
     const int row = x.lo + k0;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * MN_BOX_BYTES, mA, bar, x.m0 + j * 64, row);
+    for (int j = 0; j < 2; ++j) l2(sa + j * MN_BOX_BYTES, mA, x.m0 + j * 64, row);
 #pragma unroll
-    for (int j = j0; j < j0 + kMine; ++j) b2(sb + j * MN_BOX_BYTES, mB0, x.n0 + j * 64, row);
+    for (int j = 0; j < B_ROWS / 64; ++j) l2(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, row);
   }
 }
 
@@ -511,6 +515,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   constexpr int STAGES = Traits<KIND>::stages;
   constexpr int NBUF = Traits<KIND>::nbuf;
   constexpr int CS = Traits<KIND>::cs;
+  constexpr bool PAIR = Traits<KIND>::pair;
   constexpr int BK = Traits<KIND>::bk;
   constexpr uint32_t A_BYTES = Traits<KIND>::a_bytes;
   constexpr uint32_t B_BYTES = Traits<KIND>::b_bytes;
@@ -542,13 +547,17 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // In a pair the leader's full barriers count both CTAs' bytes, the
+    // leader's MMA commits release the stages and accumulators of both CTAs,
+    // and the leader's tempty barriers take one arrival per epilogue warp of
+    // both CTAs.
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CS);  // released by the MMA of every CTA of the cluster
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps * 32);
+      mbar_init(tempty_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
     }
     mbar_init(drain_bar, 1);
     if constexpr (Traits<KIND>::wgrad) {
@@ -568,8 +577,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     tma_prefetch_desc(&mapC1);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   // Every role decodes every tile; the offsets are read from global memory
   // once here instead of once per tile and role.
@@ -586,8 +600,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // The peer's multicasts and commits target this CTA's barriers: they must
-  // all be initialised cluster-wide first.
+  // The peer's loads, commits and arrivals target this CTA's barriers: they
+  // must all be initialised cluster-wide first.
   if constexpr (CS > 1) cluster_sync_all();
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
   const int t_first = CS > 1 ? (int)cluster_id_x() : (int)blockIdx.x;
@@ -603,6 +617,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       bool run = true;
       for (int t = t_first; run && t < total; t += t_step) {
         const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
+        // In a pair whose expert has an odd number of 128-row tiles the
+        // peer's rows all lie past the expert's end: its tile is computed
+        // but never stored, so its A rows are not loaded.
+        bool peer_idle = false;
+        if constexpr (PAIR) peer_idle = x.m0 - rank * BM + BM >= x.hi;
+        const bool load_a = !(PAIR && rank == 1 && peer_idle);
+        const uint32_t tx = PAIR ? 2 * STAGE_BYTES - (peer_idle ? A_BYTES : 0u) : STAGE_BYTES;
         for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1;
@@ -610,21 +631,33 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             run = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-          load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, full_bar(s), &mapA,
-                           &mapB0, &mapB1, rank);
+          uint32_t fb = full_bar(s);
+          if constexpr (PAIR) {
+            fb = mapa_shared(full_bar(s), 0);  // the leader's barrier counts both CTAs' bytes
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+          } else {
+            mbar_arrive_expect_tx(full_bar(s), tx);
+          }
+          load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, fb, &mapA, &mapB0, &mapB1,
+                           rank, load_a);
           issued[s] = (int)ph;
           if constexpr (Traits<KIND>::wgrad)
             if (k_tail<KIND>(x, kb).zl > 0) mbar_arrive(tail_bar(s));
         }
       }
-      // wait for every copy this thread issued before the CTA may exit
+      // Wait for every copy issued before the CTA may exit.  In a pair the
+      // leader's full barriers also count the peer's copies (the peer stays
+      // until the closing cluster barrier, which the leader reaches after
+      // this wait).
+      if (!PAIR || rank == 0) {
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s] >= 0) mbar_wait(full_bar(s), (uint32_t)issued[s], abort_flag, p.status, false);
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s] >= 0) mbar_wait(full_bar(s), (uint32_t)issued[s], abort_flag, p.status, false);
+      }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer (the leader's, in a pair) ----------------
+   if (!PAIR || rank == 0) {
     int g = 0, it = 0;
     uint32_t fixph = 0;  // bit s: parity of the next fix_bar(s) phase
     bool run = true;
@@ -632,7 +665,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * Traits<KIND>::bn;
       for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
@@ -660,27 +693,36 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           }
         }
         if (lane == 0) {
-          for (int kk = 0; kk < nk; ++kk) {
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            if (kk >= nk) break;
             const uint64_t ad = Traits<KIND>::a_mn ? desc_sw128(sa + kk * (UK * 128), MN_BOX_BYTES, 1024)
                                                    : desc_sw128(sa + kk * (UK * 2), 16, 1024);
             const uint64_t bd = Traits<KIND>::b_mn ? desc_sw128(sb + kk * (UK * 128), MN_BOX_BYTES, 1024)
                                                    : desc_sw128(sb + kk * (UK * 2), 16, 1024);
-            umma_f16(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR) umma_f16_pair(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            else umma_f16(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (CS > 1) umma_commit_mc(empty_bar(s), (uint16_t)((1u << CS) - 1u));
+          // the stage is free in both CTAs once these MMAs have read it
+          if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
           else umma_commit(empty_bar(s));
         }
         __syncwarp();
       }
       if (!run) break;
-      if (lane == 0) umma_commit(tfull_bar(acc));
+      if (lane == 0) {
+        if constexpr (PAIR) umma_commit_pair(tfull_bar(acc), 3);
+        else umma_commit(tfull_bar(acc));
+      }
       __syncwarp();
     }
     if (lane == 0) {
-      umma_commit(drain_bar);
+      if constexpr (PAIR) umma_commit_pair(drain_bar, 1);
+      else umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, abort_flag, p.status, false);
     }
     __syncwarp();
+   }
   } else if (warp < 2 + kEpiWarps) {
     // ---------------- epilogue warps 2..9 ----------------
     const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
@@ -696,7 +738,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       const uint32_t tacc = tmem_base + acc * Traits<KIND>::bn + ((uint32_t)(quarter * 32) << 16);
       epilogue<KIND>(x, p, tacc, quarter, half, lane, ring, &mapC0, &mapC1);
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if constexpr (PAIR) {
+        // one arrival per warp on the leader's barrier
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      } else {
+        mbar_arrive(tempty_bar(acc));
+      }
     }
     // the CTA's stores must be complete before it exits
     if (lane == 0) bulk_wait_group_all();
@@ -745,7 +793,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   if constexpr (CS > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -903,7 +952,7 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   const uint64_t da[2] = {(uint64_t)I, (uint64_t)N};
   const uint32_t ba[2] = {64, 128};
   const uint64_t dw[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)E};
-  const uint32_t bw[3] = {64, Traits<kFwdDown>::cs == 1 ? 256u : 128u, 1};
+  const uint32_t bw[3] = {64, (uint32_t)Traits<kFwdDown>::b_rows, 1};
   if (!make_map(&ma, A, 2, da, ba) || !make_map(&md, Wd, 3, dw, bw)) return MOE_ERR_CUDA;
   Params p = base_params(off, N, E, status);
   p.Kd = I;
