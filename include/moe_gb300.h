@@ -113,7 +113,10 @@ int moe_check_status(const int32_t* dev_status, cudaStream_t stream);
  *   row_map         [T*K] int32
  *   tokens_per_expert [E] int32, expert_offsets [E+1] int32
  *   workspace       device scratch of moe_permute_workspace_size(T, K, E)
- *                   bytes (per-block expert counts)
+ *                   bytes: ceil(T*K/512) blocks of E int32 expert counts
+ *                   (padded to 8 bytes), then one 8-byte completion flag
+ *                   per block.  Its contents need no clearing: each call
+ *                   stamps the flags with a value no earlier call used.
  *   dev_status      optional; receives MOE_ERR_BAD_ID for an id outside
  *                   [0, E + num_special) or repeated within a row (the slot
  *                   is then treated as not dispatched)
@@ -131,19 +134,21 @@ int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T,
  * reserved by another allocator (a cudaMalloc there would fail, or
  * synchronise the device at a bad moment).
  *
- * The per-block expert counts live in one file-scope device array of
+ * The workspace of moe_permute (per-block expert counts and completion
+ * flags) lives in one file-scope device array of
  * MOE_PERMUTE_STATIC_SCRATCH_INTS int32 (256 KiB) that every GPU which loads
  * this library holds until the process exits.  It is enough when
- * ceil(T*K / 512) * E <= MOE_PERMUTE_STATIC_SCRATCH_INTS; larger problems
- * return MOE_ERR_CAPACITY before anything is launched.
+ * moe_permute_workspace_size(T, K, E) <= 4 * MOE_PERMUTE_STATIC_SCRATCH_INTS,
+ * about ceil(T*K / 512) * (E + 2) int32; larger problems return
+ * MOE_ERR_CAPACITY before anything is launched.
  *   - The first call on a device looks up that device's address of the
  *     array (cudaGetSymbolAddress, with the device current); make that first
  *     call before any stream capture.
  *   - Every call uses the same array, so calls whose kernels can overlap on
  *     the GPU (different streams, no ordering between them) race with each
  *     other and must be serialised by the caller.  The array keeps the last
- *     call's contents; every entry a call reads is written by that call
- *     first, so nothing needs clearing between calls.
+ *     call's contents; a call reads only counts it wrote itself and flags
+ *     stamped with its own value, so nothing needs clearing between calls.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * Arguments and results are those of moe_permute. */
 #define MOE_PERMUTE_STATIC_SCRATCH_INTS 65536

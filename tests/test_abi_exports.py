@@ -39,7 +39,8 @@ def test_library_exports_every_header_symbol(built_lib):
         assert name in binding._SIGNATURES, f"{name} has no ctypes signature in the binding"
     assert lib.moe_abi_version() >= 1
     assert lib.moe_status_string(binding.MOE_ERR_BAD_ID) == b"expert id out of range or repeated in a row"
-    assert lib.moe_permute_workspace_size(16384, 8, 64) == 256 * 64 * 4   # 512-slot blocks
+    # 512-slot blocks: int32 expert counts per block, then one 8-byte flag per block
+    assert lib.moe_permute_workspace_size(16384, 8, 64) == 256 * 64 * 4 + 256 * 8
 
 
 def test_host_side_argument_checks_need_no_gpu(built_lib):

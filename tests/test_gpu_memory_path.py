@@ -52,6 +52,52 @@ def test_routing_bit_exact(lib, T, K, E, special):
     _routing_check(lib, _ids(T + K + E, T, K, E + special), E, special)
 
 
+def _routing_launches(lib, ids_cpu, E):
+    before = lib.moe_kernel_launches()
+    r = lib.moe_permute(None, ids_cpu.to(DEV), E, 0)
+    torch.cuda.synchronize()
+    return r, lib.moe_kernel_launches() - before
+
+
+def _assert_routing(r, ids_cpu, E):
+    si, rm, tpe, off = O.permute_routing(ids_cpu.numpy(), E)
+    assert np.array_equal(np64(r.expert_offsets), off)
+    assert np.array_equal(np64(r.tokens_per_expert), tpe)
+    assert np.array_equal(np64(r.row_map), rm)
+    assert np.array_equal(np64(r.sorted_indices)[: len(si)], si)
+
+
+def test_routing_is_one_launch_when_its_blocks_fit(lib):
+    """6147 slots, twelve 512-slot blocks: histogram, scan and stable
+    placement run as one cooperative launch."""
+    ids = _ids(11, 2049, 3, 17)
+    r, launches = _routing_launches(lib, ids, 17)
+    assert launches == 1
+    _assert_routing(r, ids, 17)
+
+
+def test_routing_three_passes_past_residency(lib):
+    """2,097,152 slots need 4096 blocks, more than the GPU holds at once: the
+    routing falls back to its three launches and stays bit exact."""
+    ids = _ids(12, 262144, 8, 64)
+    r, launches = _routing_launches(lib, ids, 64)
+    assert launches == 3
+    _assert_routing(r, ids, 64)
+
+
+def test_routing_twice_on_one_workspace(lib):
+    """The fused routing's completion flags are stamped per call, so a
+    workspace that still holds an earlier call's counts and flags (here a
+    different routing of the same size) gives the same result as a fresh
+    one."""
+    T, K, E = 3000, 8, 64
+    ws = torch.zeros(lib.moe_permute_workspace_size(T, K, E), dtype=torch.uint8, device=DEV)
+    for seed in (21, 22, 21):
+        ids = _ids(seed, T, K, E)
+        r = lib.moe_permute(None, ids.to(DEV), E, 0, workspace=ws)
+        _assert_routing(r, ids, E)
+
+
 def test_routing_empty_and_all_special(lib):
     ids = torch.zeros((0, 4), dtype=torch.int32)
     r = lib.moe_permute(None, ids.to(DEV), 8, 0)

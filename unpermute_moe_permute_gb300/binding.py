@@ -228,7 +228,8 @@ def moe_permute_static_scratch(tokens: Optional[torch.Tensor], expert_ids: torch
                                sorted_indices=None, row_map=None, tokens_per_expert=None,
                                expert_offsets=None, dev_status=None) -> PermuteResult:
     """moe_permute for callers that cannot allocate device memory: the
-    library keeps the per-block counts in its own fixed device array
+    library keeps its routing workspace (per-block counts and flags) in its
+    own fixed device array
     (MOE_PERMUTE_STATIC_SCRATCH_INTS int32), shared by every call, so calls
     must not overlap on the GPU.  Outputs the caller does not pass are
     allocated here by torch only for convenience of this binding."""

@@ -12,7 +12,11 @@
 // its K destinations with 16-byte vectors.  The rank pass is deterministic:
 // per-block counts -> per-(block, expert) bases -> per-warp bases -> in-warp
 // rank from __match_any_sync peers, so no atomic ordering reaches the output.
+#include <atomic>
+#include <chrono>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
@@ -191,6 +195,177 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int 
   }
 }
 
+// ---- the three passes above in one cooperative launch -----------------------
+//
+// For small and medium T*K the three routing kernels are bound by launch
+// latency, not by their few bytes.  This kernel runs them as phases of one
+// grid whose blocks are all resident (cooperative launch): each block counts
+// its chunk per warp (phase 1), publishes its block counts and then a flag
+// stamped with a value unique to the call, waits for every block's flag,
+// reduces the counts of all blocks itself (the totals, and the counts of
+// earlier blocks, per expert), scans the totals and places its slots exactly
+// as route_scatter_kernel does.  The stamps make stale workspace contents
+// harmless, so nothing has to be cleared before a call.  The wait is bounded:
+// on timeout the block records MOE_ERR_TIMEOUT and leaves.
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr unsigned long long kFlagWaitNs = 2000000000ull;  // 2 s
+
+__global__ void __launch_bounds__(kRouteThreads)
+route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total, SlotMask m,
+                   int32_t* __restrict__ blk_counts, unsigned long long* __restrict__ flags,
+                   unsigned long long stamp, int32_t* __restrict__ sorted_indices,
+                   int32_t* __restrict__ row_map, int32_t* __restrict__ tokens_per_expert,
+                   int32_t* __restrict__ expert_offsets, int32_t* status) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                     // [kRouteWarps][E] counts, then warp bases
+  int32_t* tot = cnt + kRouteWarps * E;  // [E] totals, then expert offsets
+  int32_t* below = tot + E;              // [E] counts of earlier blocks
+  __shared__ int32_t scan_part[kRouteThreads];
+  __shared__ int timed_out;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x, nblk = gridDim.x;
+  for (int i = tid; i < (kRouteWarps + 2) * E; i += kRouteThreads) sm[i] = 0;
+  if (tid == 0) timed_out = 0;
+  __syncthreads();
+  // 1. experts of this warp's 64 slots (kept for phase 5) and warp counts
+  const int wbase = b * kChunk + warp * kSlotsPerWarp;
+  int32_t* my = cnt + warp * E;
+  constexpr int kSteps = kSlotsPerWarp / 32;
+  int ex[kSteps];
+  bool any_bad = false;
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
+    const int f = wbase + i * 32 + lane;
+    ex[i] = -1;
+    if (f < TK) {
+      bool bad;
+      ex[i] = slot_expert(ids, f, K, E, E_total, m, &bad);
+      any_bad |= bad;
+      if (ex[i] >= 0) atomicAdd(&my[ex[i]], 1);
+    }
+  }
+  if (any_bad) set_status(status, MOE_ERR_BAD_ID);
+  __syncthreads();
+  // 2. publish the block counts, then the block's flag
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int c = 0;
+    for (int w = 0; w < kRouteWarps; ++w) c += cnt[w * E + e];
+    blk_counts[(size_t)b * E + e] = c;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) st_release_u64(&flags[b], stamp);
+  // 3. wait for every block's flag
+  for (int i = tid; i < nblk; i += kRouteThreads) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0; ld_acquire_u64(&flags[i]) != stamp; ++it) {
+      if ((it & 63u) == 63u) {
+        const unsigned long long now = global_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > kFlagWaitNs) {
+          timed_out = 1;
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (timed_out) {
+    if (tid == 0) set_status(status, MOE_ERR_TIMEOUT);
+    return;
+  }
+  // 4. per expert: total over all blocks and the counts of blocks before b
+  //    (Q threads per expert split the blocks; read through L2)
+  const int Q = E < kRouteThreads ? kRouteThreads / E : 1;
+  for (int i = tid; i < E * Q; i += kRouteThreads) {
+    const int e = i % E, q = i / E;
+    const int b_lo = (int)((long long)nblk * q / Q), b_hi = (int)((long long)nblk * (q + 1) / Q);
+    int t_sum = 0, b_sum = 0;
+    for (int bb = b_lo; bb < b_hi; ++bb) {
+      const int c = __ldcg(&blk_counts[(size_t)bb * E + e]);
+      t_sum += c;
+      if (bb < b) b_sum += c;
+    }
+    if (t_sum) atomicAdd(&tot[e], t_sum);
+    if (b_sum) atomicAdd(&below[e], b_sum);
+  }
+  __syncthreads();
+  // 5. exclusive scan of the totals over experts: thread i owns the
+  //    consecutive experts [i*per, (i+1)*per)
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += tot[e];
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) scan_part[warp] = incl;
+  __syncthreads();
+  int wprefix = 0;
+  for (int w = 0; w < warp; ++w) wprefix += scan_part[w];
+  int run = wprefix + incl - local;  // exclusive prefix of expert e0
+  __syncthreads();
+  for (int e = e0; e < e1; ++e) {
+    const int c = tot[e];
+    if (b == 0) {
+      tokens_per_expert[e] = c;
+      expert_offsets[e] = run;
+    }
+    tot[e] = run;
+    run += c;
+  }
+  if (b == 0 && e1 == E && e0 < e1) expert_offsets[E] = run;
+  __syncthreads();
+  // 6. warp bases: expert offset + earlier blocks + earlier warps of this block
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int r = tot[e] + below[e];
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = r;
+      r += c;
+    }
+  }
+  __syncthreads();
+  // 7. stable rank inside each 32-slot step (as in route_scatter_kernel)
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
+    const int f = wbase + i * 32 + lane;
+    const int e = ex[i];
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lanemask_lt());
+    if (e >= 0) {
+      const int pos = my[e] + rank;
+      sorted_indices[pos] = f;
+      row_map[f] = pos;
+    } else if (f < TK) {
+      row_map[f] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 // One warp per token: read the row once (16-byte vectors), write it to each
 // of its K permuted rows.
 template <int kUnroll>
@@ -245,6 +420,48 @@ __global__ void invert_kernel(const int32_t* __restrict__ sorted_indices, int N,
 
 static inline int route_blocks(int TK) { return (TK + kChunk - 1) / kChunk; }
 
+// Workspace: per-block expert counts [nblk][E] int32, then (8-byte aligned)
+// the per-block flags of the fused routing [nblk] uint64.
+static inline size_t flags_offset(long long nblk, int E) {
+  return (size_t)((nblk * E * (long long)sizeof(int32_t) + 7) & ~7LL);
+}
+
+static inline size_t fused_smem_bytes(int E) { return (size_t)(kRouteWarps + 2) * E * sizeof(int32_t); }
+
+// Whether nblk blocks of the fused routing kernel fit on the current device
+// at once (cooperative launch); cached per (device, E).
+static bool fused_fits(int nblk, int E) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> cap;  // (device, E) -> resident blocks
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cap.find({dev, E});
+  if (it == cap.end()) {
+    int coop = 0, per_sm = 0;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_fused_kernel, kRouteThreads,
+                                                      fused_smem_bytes(E)) == cudaSuccess)
+      n = per_sm * sm_count();
+    (void)cudaGetLastError();
+    it = cap.emplace(std::make_pair(dev, E), n).first;
+  }
+  return nblk <= it->second;
+}
+
+// A value no earlier call of this process used (and, being seeded from the
+// clock, very unlikely to be found in a fresh workspace).
+static unsigned long long next_stamp() {
+  static std::atomic<unsigned long long> counter{
+      ((unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() << 20) | 1ull};
+  unsigned long long v;
+  do {
+    v = counter.fetch_add(1ull);
+  } while (v == 0ull);
+  return v;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -252,8 +469,8 @@ using namespace moe;
 extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
   if (T < 0 || K <= 0 || E <= 0) return 0;
   const long long TK = (long long)T * K;
-  const long long nblk = (TK + kChunk - 1) / kChunk;
-  return (size_t)((nblk > 0 ? nblk : 1) * E * sizeof(int32_t));
+  const long long nblk = (TK + kChunk - 1) / kChunk > 0 ? (TK + kChunk - 1) / kChunk : 1;
+  return flags_offset(nblk, E) + (size_t)nblk * sizeof(unsigned long long);
 }
 
 extern "C" int moe_permute_masked(const void* tokens, int dtype, const int32_t* expert_ids, int T,
@@ -292,16 +509,36 @@ extern "C" int moe_permute_masked(const void* tokens, int dtype, const int32_t* 
   int32_t* blk = static_cast<int32_t*>(workspace);
   const int E_total = E + num_special;
   const SlotMask m{active_mask, mask_dims};
-  route_hist_kernel<<<nblk, kRouteThreads, E * sizeof(int32_t), stream>>>(expert_ids, TK, K, E,
-                                                                         E_total, m, blk, dev_status);
-  route_scan_kernel<<<1, 1024, 0, stream>>>(blk, nblk, E, tokens_per_expert, expert_offsets);
-  const size_t scatter_smem = (size_t)kRouteWarps * E * sizeof(int32_t);
-  if (scatter_smem > 48 * 1024)
-    cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)scatter_smem);
-  route_scatter_kernel<<<nblk, kRouteThreads, scatter_smem, stream>>>(
-      expert_ids, TK, K, E, E_total, m, blk, sorted_indices, row_map);
-  count_launches(3);
+  bool fused = false;
+  if (fused_fits(nblk, E)) {
+    // all blocks resident: the three routing passes as one launch
+    unsigned long long* flags =
+        reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + flags_offset(nblk, E));
+    unsigned long long stamp = next_stamp();
+    void* args[] = {(void*)&expert_ids, (void*)&TK, (void*)&K, (void*)&E, (void*)&E_total,
+                    (void*)&m, (void*)&blk, (void*)&flags, (void*)&stamp, (void*)&sorted_indices,
+                    (void*)&row_map, (void*)&tokens_per_expert, (void*)&expert_offsets,
+                    (void*)&dev_status};
+    if (cudaLaunchCooperativeKernel((const void*)route_fused_kernel, dim3(nblk), dim3(kRouteThreads),
+                                    args, fused_smem_bytes(E), stream) == cudaSuccess) {
+      fused = true;
+      count_launches(1);
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
+  if (!fused) {
+    route_hist_kernel<<<nblk, kRouteThreads, E * sizeof(int32_t), stream>>>(
+        expert_ids, TK, K, E, E_total, m, blk, dev_status);
+    route_scan_kernel<<<1, 1024, 0, stream>>>(blk, nblk, E, tokens_per_expert, expert_offsets);
+    const size_t scatter_smem = (size_t)kRouteWarps * E * sizeof(int32_t);
+    if (scatter_smem > 48 * 1024)
+      cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)scatter_smem);
+    route_scatter_kernel<<<nblk, kRouteThreads, scatter_smem, stream>>>(
+        expert_ids, TK, K, E, E_total, m, blk, sorted_indices, row_map);
+    count_launches(3);
+  }
   if (tokens != nullptr && T > 0) {
     const int row_bytes = H * dtype_size(dtype);
     permute_rows_kernel<4><<<(T + 7) / 8, 256, 0, stream>>>(
