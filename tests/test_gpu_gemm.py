@@ -37,6 +37,12 @@ SMALL = [
     dict(T=700, H=320, E=16, K=8, I=128),     # 3 m-tiles per expert, partial 256-column down tile
     dict(T=64, H=128, E=64, K=2, I=64),       # many experts without rows
     dict(T=1, H=64, E=4, K=1, I=64),          # a single row
+    # about 1950 rows per expert: gate/up runs as CTA pairs (odd and even
+    # per-expert tile counts), down single
+    dict(T=2600, H=256, E=4, K=3, I=192),
+    # about 2250 rows per expert: both forward GEMMs run as CTA pairs,
+    # partial 256-column down tile
+    dict(T=4500, H=320, E=4, K=2, I=128),
 ]
 
 

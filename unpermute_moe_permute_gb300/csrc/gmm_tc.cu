@@ -60,12 +60,15 @@ enum Kind : int {
   kWgradDown = 4,
   kWgradGateUp = 5,
 };
+// A kernel variant is a Kind, plus kPaired for the CTA-pair form.
+constexpr int kPaired = 8;
+constexpr int kind_of(int variant) { return variant & 7; }
 
 template <int KIND>
 struct Traits {
-  static constexpr bool a_mn = (KIND == kWgradDown || KIND == kWgradGateUp);
-  static constexpr bool b_mn = (KIND >= kDgradDown);
-  static constexpr bool wgrad = (KIND == kWgradDown || KIND == kWgradGateUp);
+  static constexpr bool a_mn = (kind_of(KIND) == kWgradDown || kind_of(KIND) == kWgradGateUp);
+  static constexpr bool b_mn = (kind_of(KIND) >= kDgradDown);
+  static constexpr bool wgrad = (kind_of(KIND) == kWgradDown || kind_of(KIND) == kWgradGateUp);
   // TMA producer, MMA issuer, epilogue warps, and for the wgrads one warp
   // that zeroes the rows past an expert's end in its last k block, so that
   // the MMA-issuing warp only issues.
@@ -75,19 +78,19 @@ struct Traits {
   // its epilogue, not by idle SMs).
   static constexpr int bn = 256;
   static constexpr int pieces = bn / 32;  // 32-column epilogue pieces per tile
-  static constexpr int n_per_tile = (KIND == kFwdGateUp) ? bn / 2 : bn;  // output columns
+  static constexpr int n_per_tile = (kind_of(KIND) == kFwdGateUp) ? bn / 2 : bn;  // output columns
   // CTA pairs (cta_group::2): the two CTAs of a cluster take vertically
   // adjacent 128-row tiles of one expert and n tile and hold half of the
   // B tile each, so per SM the MMA reads and the TMA writes 32 KB of shared
-  // memory per k block instead of 48 KB.  The price is a wasted half tile
-  // for every expert with an odd number of 128-row tiles.  Measured at
-  // T=4096 H=2048 E=128 K=8 I=768 (same GPU, back to back, us):
-  //   gate_up 204 pair / 207 single, down 107 / 108,
-  //   down dgrad 160 / 150, gate_up dgrad 196 / 195,
-  // so pairs are used for the forward kinds.  The wgrads stay single: their
+  // memory per k block instead of 48 KB, which leaves room for a 6-stage
+  // ring.  The price is a wasted half tile for every expert with an odd
+  // number of 128-row tiles, so whether a call runs paired is decided per
+  // call from the rows per expert (use_pairs).  The dgrads measured no
+  // better paired at the layer shapes, and the wgrads stay single: their
   // expert tail rows are zeroed in shared memory after the loads land,
   // which the leader cannot observe for the peer's loads.
-  static constexpr bool pair = (KIND == kFwdGateUp || KIND == kFwdDown);
+  static constexpr bool pair = (KIND & kPaired) != 0;
+  static_assert(!(pair && wgrad), "the wgrad tail fix-up is single-CTA");
   static constexpr int cs = pair ? 2 : 1;  // CTAs per cluster
   static constexpr int b_rows = pair ? bn / 2 : bn;  // B rows (N) this CTA holds
   static constexpr uint32_t idesc = idesc_bf16_f32(BM * cs, bn, a_mn, b_mn);
@@ -99,14 +102,13 @@ struct Traits {
   static constexpr int bk = 64;
   // The SwiGLU-backward epilogue stages two units (dg, du) per piece and is
   // the slower side of its kernel: it trades a stage for a two-unit ring.
-  static constexpr int nbuf = KIND == kDgradDown ? 2 : 1;
-  static constexpr int stages = pair ? (KIND == kDgradDown ? 5 : 6) : (KIND == kDgradDown ? 3 : 4);
+  static constexpr int nbuf = kind_of(KIND) == kDgradDown ? 2 : 1;
+  static constexpr int stages = pair ? (kind_of(KIND) == kDgradDown ? 5 : 6) : (kind_of(KIND) == kDgradDown ? 3 : 4);
   static constexpr uint32_t a_bytes = BM * bk * 2;
   static constexpr uint32_t b_bytes = b_rows * bk * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
   static constexpr uint32_t mn_box = 64 * bk * 2;  // one 64 (M/N) x bk (K) MN-major box
   static_assert(stages <= kMaxStages, "more stages than the control block holds");
-  static_assert(!(pair && wgrad), "the wgrad tail fix-up is single-CTA");
   static constexpr uint32_t staging_bytes = kEpiWarps * nbuf * UNIT_BYTES;
   static constexpr uint32_t smem_bytes = stages * stage_bytes + staging_bytes + CTRL_BYTES + 1024;
   static_assert(smem_bytes <= 232448, "more shared memory than one CTA may use");
@@ -212,7 +214,7 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
     else tma_load_3d(dst, m, bar, bx, by, bz);
   };
   const int nb = x.n0 + (PAIR ? rank * B_ROWS : 0);  // first B row (N) of this CTA's part
-  if constexpr (KIND == kFwdGateUp) {
+  if constexpr (kind_of(KIND) == kFwdGateUp) {
     // B tile = 128 rows of W_gate, then the same 128 rows of W_up
     if (load_a) l2(sa, mA, k0, x.m0);
     if constexpr (PAIR) {
@@ -221,14 +223,14 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
       l3(sb, mB0, k0, x.n0, x.e);
       l3(sb + Traits<KIND>::b_bytes / 2, mB1, k0, x.n0, x.e);
     }
-  } else if constexpr (KIND == kFwdDown) {
+  } else if constexpr (kind_of(KIND) == kFwdDown) {
     if (load_a) l2(sa, mA, k0, x.m0);
     l3(sb, mB0, k0, nb, x.e);  // B_ROWS rows of the W_down panel in one box
-  } else if constexpr (KIND == kDgradDown) {
+  } else if constexpr (kind_of(KIND) == kDgradDown) {
     if (load_a) l2(sa, mA, k0, x.m0);
 #pragma unroll
     for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, k0, x.e);
-  } else if constexpr (KIND == kDgradGateUp) {
+  } else if constexpr (kind_of(KIND) == kDgradGateUp) {
     if (load_a) l2(sa, mA, k0, x.m0);
     const bool up = k0 >= p.I;
     const int kk = up ? k0 - p.I : k0;
@@ -350,7 +352,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
     const bool full = r0 + 32 <= x.hi;
     const int row = r0 + lane;
     const bool rv = row < x.hi;
-    if constexpr (KIND == kFwdGateUp) {
+    if constexpr (kind_of(KIND) == kFwdGateUp) {
       const int I = p.Nout;
 #pragma unroll 1
       for (int c = 2 * half; c < 2 * half + 2; ++c) {
@@ -384,7 +386,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
                             (!full && rv) ? p.save + (size_t)row * 2 * I + I + col : nullptr);
         }
       }
-    } else if constexpr (KIND == kFwdDown || KIND == kDgradGateUp) {
+    } else if constexpr (kind_of(KIND) == kFwdDown || kind_of(KIND) == kDgradGateUp) {
       constexpr int HP = Traits<KIND>::pieces / 2;
 #pragma unroll 1
       for (int c = HP * half; c < HP * half + HP; ++c) {
@@ -478,7 +480,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
     if (r0 >= p.Mout) return;
     const CUtensorMap* map = mC0;
     int y = r0;
-    if constexpr (KIND == kWgradGateUp) {
+    if constexpr (kind_of(KIND) == kWgradGateUp) {
       if (r0 >= p.I) {
         map = mC1;
         y = r0 - p.I;
@@ -894,6 +896,23 @@ int device_ok() {
   return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
+// Whether a forward GEMM runs as CTA pairs, from the rows per expert.  A
+// pair wastes half a tile on every expert with an odd number of 128-row
+// tiles, and skewed routing has many of them.  GB300, H=2048, bf16, us,
+// pair / single:
+//   routing     rows/expert   gate/up (I=768|512)   down
+//   uniform         256         202 / 210          108 / 108
+//   uniform         512         318 / 323          167 / 172
+//   uniform        1024         562 / 577          289 / 304
+//   uniform        2048        1028 / 1069         531 / 569
+//   Zipf(1.2)       256         301 / 289          179 / 159
+//   Zipf(1.2)      1024         742 / 780          455 / 442
+// Gate/up pairs from 512 rows per expert, down pairs from 2048, so that
+// skewed routing never pays for them.
+constexpr long long kPairMinRowsGateUp = 512;
+constexpr long long kPairMinRowsDown = 2048;
+inline bool use_pairs(long long min_rows, int N, int E) { return (long long)N >= min_rows * E; }
+
 Params base_params(const int32_t* off, int N, int E, int32_t* status) {
   Params p{};
   p.off = off;
@@ -942,7 +961,9 @@ int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const
   CUtensorMap c_act, c_save;
   if (!store_map_2d(&c_act, act, I, N) || !store_map_2d(&c_save, save ? save : act, save ? 2 * I : I, N))
     return MOE_ERR_CUDA;
-  return launch<kFwdGateUp>(ma, mg, mu, c_act, c_save, p, s);
+  return use_pairs(kPairMinRowsGateUp, N, E)
+             ? launch<kFwdGateUp | kPaired>(ma, mg, mu, c_act, c_save, p, s)
+             : launch<kFwdGateUp>(ma, mg, mu, c_act, c_save, p, s);
 }
 
 int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int N, int H, int I,
@@ -952,7 +973,9 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   const uint64_t da[2] = {(uint64_t)I, (uint64_t)N};
   const uint32_t ba[2] = {64, 128};
   const uint64_t dw[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)E};
-  const uint32_t bw[3] = {64, (uint32_t)Traits<kFwdDown>::b_rows, 1};
+  const bool paired = use_pairs(kPairMinRowsDown, N, E);
+  const uint32_t bw[3] = {64, (uint32_t)(paired ? Traits<kFwdDown | kPaired>::b_rows
+                                                : Traits<kFwdDown>::b_rows), 1};
   if (!make_map(&ma, A, 2, da, ba) || !make_map(&md, Wd, 3, dw, bw)) return MOE_ERR_CUDA;
   Params p = base_params(off, N, E, status);
   p.Kd = I;
@@ -962,7 +985,8 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   p.out = static_cast<__nv_bfloat16*>(out);
   CUtensorMap c_out;
   if (!store_map_2d(&c_out, out, H, N)) return MOE_ERR_CUDA;
-  return launch<kFwdDown>(ma, md, md, c_out, c_out, p, s);
+  return paired ? launch<kFwdDown | kPaired>(ma, md, md, c_out, c_out, p, s)
+                : launch<kFwdDown>(ma, md, md, c_out, c_out, p, s);
 }
 
 int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* off, int N, int H,
