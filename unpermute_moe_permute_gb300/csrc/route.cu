@@ -145,6 +145,7 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int 
                      const int32_t* __restrict__ blk_base, int32_t* __restrict__ sorted_indices,
                      int32_t* __restrict__ row_map) {
   extern __shared__ int32_t cnt[];  // [kRouteWarps][E]
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = threadIdx.x; i < kRouteWarps * E; i += kRouteThreads) cnt[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,6 +241,8 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
   __shared__ int timed_out;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, nblk = gridDim.x;
+  // the row copy may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = tid; i < (kRouteWarps + 2) * E; i += kRouteThreads) sm[i] = 0;
   if (tid == 0) timed_out = 0;
   __syncthreads();
@@ -298,6 +301,7 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
     const int e = i % E, q = i / E;
     const int b_lo = (int)((long long)nblk * q / Q), b_hi = (int)((long long)nblk * (q + 1) / Q);
     int t_sum = 0, b_sum = 0;
+#pragma unroll 8
     for (int bb = b_lo; bb < b_hi; ++bb) {
       const int c = __ldcg(&blk_counts[(size_t)bb * E + e]);
       t_sum += c;
@@ -372,6 +376,9 @@ template <int kUnroll>
 __global__ void __launch_bounds__(256)
 permute_rows_kernel(const uint8_t* __restrict__ tokens, const int32_t* __restrict__ row_map, int T,
                     int K, int row_bytes, uint8_t* __restrict__ permuted) {
+  // Launched as a programmatic dependent of the routing: wait until that
+  // grid has completed and its row_map is visible (a no-op otherwise).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -541,9 +548,21 @@ extern "C" int moe_permute_masked(const void* tokens, int dtype, const int32_t* 
   }
   if (tokens != nullptr && T > 0) {
     const int row_bytes = H * dtype_size(dtype);
-    permute_rows_kernel<4><<<(T + 7) / 8, 256, 0, stream>>>(
-        static_cast<const uint8_t*>(tokens), row_map, T, K, row_bytes,
-        static_cast<uint8_t*>(permuted));
+    // Programmatic dependent launch: the copy's launch overlaps the routing.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((T + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const uint8_t* tok = static_cast<const uint8_t*>(tokens);
+    uint8_t* dst = static_cast<uint8_t*>(permuted);
+    const int32_t* rm = row_map;
+    if (cudaLaunchKernelEx(&cfg, permute_rows_kernel<4>, tok, rm, T, K, row_bytes, dst) != cudaSuccess)
+      return MOE_ERR_CUDA;
     count_launches(1);
   }
   MOE_LAUNCH_CHECK();
