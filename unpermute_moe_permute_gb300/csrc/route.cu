@@ -49,7 +49,8 @@ __device__ __forceinline__ int slot_expert(const int32_t* __restrict__ ids, int 
   const int id = ids[f];
   const int row0 = (f / K) * K;
   bool ok = (id >= 0) && (id < E_total);
-  for (int j = row0; j < f; ++j) ok = ok && (ids[j] != id);
+  // no short-circuit: the loads of the earlier ids of the row are independent
+  for (int j = row0; j < f; ++j) ok &= (ids[j] != id);
   *bad = !ok;
   return (ok && id < E && m.active(f, K)) ? id : -1;
 }
