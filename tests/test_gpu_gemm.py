@@ -75,6 +75,30 @@ def test_bf16_expert_mlp_zipf_skew(lib):
     assert_normwise(np64(expanded)[:N], w_exp, BF16_TOL, "expanded")
 
 
+def test_bf16_expert_mlp_paired_with_tiny_and_empty_experts(lib):
+    """About 2048 rows per expert on average, so both forward GEMMs run as
+    CTA pairs, but one expert has 5 rows (a single 128-row tile: the peer
+    CTA's rows are all past the expert's end) and one has none."""
+    d = moe_inputs.layer_fwd_bwd(3, T=8192, H=256, E=8, K=2, I=128)
+    rng = np.random.Generator(np.random.PCG64(3))
+    ids = moe_inputs.uniform_distinct_ids(rng, 8192, 2, 6)      # experts 0..5 only
+    ids[:5, 1] = 7                                                # expert 7: 5 rows, expert 6: none
+    d["expert_ids"] = ids
+    r = lib.moe_permute(d["tokens"].to(DEV), ids.to(DEV), d["E"], 0)
+    Wg, Wu, Wd = _weights(d)
+    act, expanded, gu = lib.moe_expert_mlp(r.permuted, r.expert_offsets, Wg, Wu, Wd, save=True)
+    (si, rm, tpe, off), perm, w_act, w_exp, g, u = _oracle_forward(d)
+    N, I = len(si), d["I"]
+    assert tpe[6] == 0 and tpe[7] == 5 and N == 8192 * 2
+    assert_normwise(np64(gu)[:N, :I], O.round_to_bf16(g), BF16_TOL, "gate")
+    assert_normwise(np64(gu)[:N, I:], O.round_to_bf16(u), BF16_TOL, "up")
+    assert_normwise(np64(act)[:N], w_act, BF16_TOL, "act")
+    assert_normwise(np64(expanded)[:N], w_exp, BF16_TOL, "expanded")
+    # the tiny expert's rows on their own
+    lo = int(off[7])
+    assert_normwise(np64(expanded)[lo:lo + 5], w_exp[lo:lo + 5], BF16_TOL, "tiny expert")
+
+
 def _sub_forward(perm_rows, experts, d):
     """Oracle forward of selected permuted rows (rows are independent given
     their expert): a sub-problem whose offsets group the rows by expert."""
