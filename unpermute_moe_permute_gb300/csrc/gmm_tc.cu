@@ -14,7 +14,11 @@
 //   * warps 2-9 (two per TMEM lane quarter, each taking half of the
 //     columns) drain an accumulator with tcgen05.ld while the next tile
 //     accumulates into the other one, apply the epilogue, stage bf16 in
-//     shared memory and write it with TMA stores.
+//     shared memory and write it with TMA stores;
+//   * the wgrads add a warp that zeroes expert tail rows in shared memory;
+//   * the forward kinds also come as CTA pairs (tcgen05 cta_group::2, a
+//     2-CTA cluster on one TPC, M=256 per MMA, half of the B tile per CTA,
+//     6-stage ring), chosen per call from the rows per expert.
 //
 // Six variants (KIND) share the machinery:
 //   FwdGateUp   act = silu(X Wg^T) * (X Wu^T)       B tile = 128 rows of Wg
@@ -157,7 +161,7 @@ __device__ __forceinline__ KTail k_tail(const Tile& x, int kb) {
   return r;
 }
 
-// Cluster tile t: a group of CS vertically adjacent 128-row tiles of one
+// Tile t: a group of CS (1, or 2 for a pair) vertically adjacent 128-row tiles of one
 // expert and one n tile; this CTA (cluster rank `rank`) takes the rank-th.
 // A rank whose rows lie past the expert's end computes a tile that is never
 // stored (its loads read the next expert's rows, or zeros past the buffer).
@@ -773,11 +777,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
         tph ^= 1u << s;
         const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
-        // lane i zeroes 16-byte chunk (i & 7) of tail row z0 + (i >> 3) in
+        // lane c zeroes 16-byte chunk (c & 7) of tail row z0 + (c >> 3) in
         // all six operand boxes (2 of A, 4 of B); the rows are 128 bytes and
         // the 128-byte swizzle only permutes chunks within a row
-        for (int i = lane; i < kt.zl * 8; i += 32) {
-          const uint32_t off = (uint32_t)(kt.z0 + (i >> 3)) * 128u + (uint32_t)(i & 7) * 16u;
+        for (int c = lane; c < kt.zl * 8; c += 32) {
+          const uint32_t off = (uint32_t)(kt.z0 + (c >> 3)) * 128u + (uint32_t)(c & 7) * 16u;
 #pragma unroll
           for (int box = 0; box < 2; ++box) st_shared_v4(sa + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
 #pragma unroll
