@@ -304,24 +304,27 @@ class PermuteUnpermute:
         return out, gt, gprob
 
 
-def _gemm_bytes(T, H, E_active, E, K, I, bf=2):
+def _gemm_bytes(T, H, E_active, E, K, I, bf=2, fused=False):
     """Algorithmic bytes and flops of each call of the bf16 layer (each
     operand read once, each result written once; weights of experts that
-    have rows are read, weight grads of every expert are written)."""
+    have rows are read, weight grads of every expert are written).  fused:
+    the permute only routes, and the gate/up GEMMs read the [T, H] token
+    matrix (their gathered operand) instead of the [N, H] permuted copy."""
     N = T * K
     idx = N * 4
     w_gu, w_d = E_active * 2 * I * H * bf, E_active * H * I * bf
+    x_rows = T if fused else N  # rows of the gate/up GEMMs' token operand
     by = {
-        "permute": T * H * bf + N * H * bf + 4 * idx,
-        "gate_up_swiglu": N * H * bf + w_gu + N * I * bf + N * 2 * I * bf,
-        "gate_up_swiglu_nosave": N * H * bf + w_gu + N * I * bf,
+        "permute": 4 * idx if fused else T * H * bf + N * H * bf + 4 * idx,
+        "gate_up_swiglu": x_rows * H * bf + w_gu + N * I * bf + N * 2 * I * bf,
+        "gate_up_swiglu_nosave": x_rows * H * bf + w_gu + N * I * bf,
         "down_proj": N * I * bf + w_d + N * H * bf,
         "unpermute": N * H * bf + T * H * bf + idx + N * 4,
         "unpermute_grad": T * H * bf + 2 * N * H * bf + idx + 2 * N * 4,
         "down_dgrad_swiglu": N * H * bf + w_d + 2 * N * 2 * I * bf,
         "gate_up_dgrad": N * 2 * I * bf + w_gu + N * H * bf,
         "down_wgrad": N * H * bf + N * I * bf + E * H * I * bf,
-        "gate_up_wgrad": N * 2 * I * bf + N * H * bf + E * 2 * I * H * bf,
+        "gate_up_wgrad": N * 2 * I * bf + x_rows * H * bf + E * 2 * I * H * bf,
         "permute_grad": N * H * bf + T * H * bf + idx,
     }
     fl = {
@@ -341,6 +344,10 @@ class LayerFwdBwd:
 
     name = "layer_fwd_bwd"
     oracle_start_tokens = 256  # amortises the oracle's per-expert weight reads
+    # True: the permute's row copy fused into the gate/up GEMMs (they gather
+    # the token rows themselves).  Off by default: on GB300 at these shapes
+    # the gathering GEMMs are slower than the row copy plus the plain GEMMs.
+    FUSED_PERMUTE = False
 
     @staticmethod
     def available(lib):
@@ -349,6 +356,7 @@ class LayerFwdBwd:
     def __init__(self, lib, dev, seed=0, gen=moe_inputs.layer_fwd_bwd, backward=True, **kw):
         d = gen(seed, **kw)
         self.lib, self.dev, self.backward = lib, dev, backward
+        self.fused = self.FUSED_PERMUTE
         T, H, E, K, I = d["T"], d["H"], d["E"], d["K"], d["I"]
         self.T, self.H, self.E, self.K, self.I = T, H, E, K, I
         keys = ("tokens", "expert_ids", "probs") + (("grad_out",) if backward else ())
@@ -358,7 +366,8 @@ class LayerFwdBwd:
         N = T * K
         bf = torch.bfloat16
         e = lambda *shape, dt=bf: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
-        self.permuted, self.sorted, self.row_map = e(N, H), e(N, dt=torch.int32), e(N, dt=torch.int32)
+        self.permuted = None if self.fused else e(N, H)
+        self.sorted, self.row_map = e(N, dt=torch.int32), e(N, dt=torch.int32)
         self.tpe, self.off = e(E, dt=torch.int32), e(E + 1, dt=torch.int32)
         self.ws = e(max(lib.moe_permute_workspace_size(T, K, E), 16), dt=torch.uint8)
         self.act, self.expanded, self.out = e(N, I), e(N, H), e(T, H)
@@ -369,13 +378,15 @@ class LayerFwdBwd:
             self.gtok = e(T, H)
         counts = np.bincount(d["expert_ids"].numpy().reshape(-1), minlength=E)
         self.E_active = int((counts > 0).sum())
-        by, fl = _gemm_bytes(T, H, self.E_active, E, K, I)
+        by, fl = _gemm_bytes(T, H, self.E_active, E, K, I, fused=self.fused)
         if not backward:
             by["gate_up_swiglu"], fl["gate_up_swiglu"] = by["gate_up_swiglu_nosave"], fl["gate_up_swiglu_nosave"]
         self.bytes, self.flops = by, fl
         self.config = {"workload": f"{'layer_fwd_bwd' if backward else 'layer_forward'}: "
                                    f"T={T} H={H} E={E} K={K} I={I} bf16, fp32 probs",
                        "T": T, "H": H, "E": E, "K": K, "I": I, "experts_with_rows": self.E_active,
+                       "permute": ("routing only; the gate/up GEMMs gather the token rows "
+                                   "(TMA row gathers)") if self.fused else "routing + row copy",
                        "l2": "inputs larger than L2 (weights alone exceed it), no flush"}
 
     @classmethod
@@ -394,12 +405,17 @@ class LayerFwdBwd:
         lib, x = self.lib, (x or self.x)
         T, K, E = self.T, self.K, self.E
         with t("permute"):
-            lib.moe_permute(x["tokens"], x["expert_ids"], E, 0, permuted=self.permuted,
-                            sorted_indices=self.sorted, row_map=self.row_map,
-                            tokens_per_expert=self.tpe, expert_offsets=self.off, workspace=self.ws)
+            lib.moe_permute(None if self.fused else x["tokens"], x["expert_ids"], E, 0,
+                            permuted=self.permuted, sorted_indices=self.sorted,
+                            row_map=self.row_map, tokens_per_expert=self.tpe,
+                            expert_offsets=self.off, workspace=self.ws)
         with t("gate_up_swiglu"):
-            lib.moe_gate_up_swiglu(self.permuted, self.off, self.Wg, self.Wu, act=self.act,
-                                   gate_up_save=self.gu)
+            if self.fused:
+                lib.moe_gate_up_swiglu_gather(x["tokens"], self.sorted, K, self.off, self.Wg,
+                                              self.Wu, act=self.act, gate_up_save=self.gu)
+            else:
+                lib.moe_gate_up_swiglu(self.permuted, self.off, self.Wg, self.Wu, act=self.act,
+                                       gate_up_save=self.gu)
         with t("down_proj"):
             lib.moe_down_proj(self.act, self.off, self.Wd, expanded=self.expanded)
         with t("unpermute"):
@@ -416,7 +432,12 @@ class LayerFwdBwd:
         with t("down_wgrad"):
             lib.moe_down_wgrad(self.gexp, self.act, self.off, dW_down=self.dWd)
         with t("gate_up_wgrad"):
-            lib.moe_gate_up_wgrad(self.dgu, self.permuted, self.off, dW_gate=self.dWg, dW_up=self.dWu)
+            if self.fused:
+                lib.moe_gate_up_wgrad_gather(self.dgu, x["tokens"], self.sorted, K, self.off,
+                                             dW_gate=self.dWg, dW_up=self.dWu)
+            else:
+                lib.moe_gate_up_wgrad(self.dgu, self.permuted, self.off, dW_gate=self.dWg,
+                                      dW_up=self.dWu)
         with t("permute_grad"):
             lib.moe_permute_grad(self.dperm, self.row_map, T, K, out=self.gtok)
 
@@ -784,7 +805,12 @@ def main(argv=None):
     ap.add_argument("--workload", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--fused-permute", action="store_true",
+                    help="layer workloads: the gate/up GEMMs gather the token rows themselves "
+                         "(default: the permute writes the permuted copy they read)")
     args = ap.parse_args(argv)
+    if args.fused_permute:
+        LayerFwdBwd.FUSED_PERMUTE = True
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = dist_env()

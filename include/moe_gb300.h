@@ -203,6 +203,35 @@ int moe_expert_mlp(const void* permuted, int dtype, const int32_t* expert_offset
                    void* act, void* expanded, void* gate_up_save, int32_t* dev_status,
                    cudaStream_t stream);
 
+/* ---- the permute fused into the gate/up GEMMs (bf16) --------------------
+ *
+ * The twinkle PR "NPU EP experts forward uses NPU grouped matmul" feeds the
+ * grouped matmul with x[permuted_indices], a gathered copy of the tokens.
+ * These two calls give exactly what moe_gate_up_swiglu and
+ * moe_gate_up_wgrad give on that copy,
+ *   permuted[i] = tokens[sorted_indices[i] / K]      (i < expert_offsets[E]),
+ * but read its rows straight from the token matrix (16-byte cp.async copies
+ * by the GEMMs' producer warp), so neither the permute's row copy nor the [N, H]
+ * permuted buffer is needed: run moe_permute with tokens = NULL for
+ * sorted_indices and expert_offsets.
+ *   tokens          [T, H] bf16 (T >= 1 when N > 0)
+ *   sorted_indices  [N] int32 from moe_permute (its first expert_offsets[E]
+ *                   entries are read; an entry outside [0, T*K) reads token
+ *                   row 0 instead of faulting)
+ *   K               slots per token of that routing (1 <= K <= 16)
+ * Other arguments as moe_gate_up_swiglu / moe_gate_up_wgrad (bf16 only;
+ * the gathering kernels are single-CTA).  Returns MOE_ERR_UNSUPPORTED for
+ * fp32, MOE_ERR_INVALID_ARG for a NULL or misaligned pointer or bad T, K.
+ */
+int moe_gate_up_swiglu_gather(const void* tokens, int T, const int32_t* sorted_indices, int K,
+                              const int32_t* expert_offsets, int N, int H, int I, int E,
+                              const void* W_gate, const void* W_up, void* act,
+                              void* gate_up_save, int32_t* dev_status, cudaStream_t stream);
+int moe_gate_up_wgrad_gather(const void* dgu, const void* tokens, int T,
+                             const int32_t* sorted_indices, int K, const int32_t* expert_offsets,
+                             int N, int H, int I, int E, void* dW_gate, void* dW_up,
+                             int32_t* dev_status, cudaStream_t stream);
+
 /* ---- unpermute forward / backward (Ascend/pytorch PR "Update moe token
  * unpermute DTensor support": tokens shard on H, the probs grad is a sum
  * over H) -----------------------------------------------------------------

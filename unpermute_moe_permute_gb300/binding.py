@@ -78,6 +78,8 @@ _SIGNATURES = {
     "moe_gate_up_dgrad": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_down_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_gate_up_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_gate_up_swiglu_gather": ([_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_gate_up_wgrad_gather": ([_P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
 }
 
 
@@ -361,6 +363,41 @@ def moe_gate_up_wgrad(dgu, permuted, expert_offsets, *, dW_gate, dW_up, dev_stat
     E, I, _ = dW_gate.shape
     _call("moe_gate_up_wgrad", _ptr(dgu), _ptr(permuted), _dtype(permuted), _ptr(expert_offsets),
           N, H, I, E, _ptr(dW_gate), _ptr(dW_up), _ptr(dev_status), _stream())
+    return dW_gate, dW_up
+
+
+def moe_gate_up_swiglu_gather(tokens, sorted_indices, K: int, expert_offsets, W_gate, W_up, *,
+                              N: Optional[int] = None, act=None, gate_up_save=None,
+                              save: bool = False, dev_status=None):
+    """moe_gate_up_swiglu of tokens[sorted_indices[i] // K] without building
+    that permuted copy: the GEMM gathers the token rows itself (bf16)."""
+    _check(tokens, torch.bfloat16, "tokens")
+    _check(sorted_indices, torch.int32, "sorted_indices")
+    T, H = tokens.shape
+    N = sorted_indices.shape[0] if N is None else N
+    E, I, _ = W_gate.shape
+    if act is None:
+        act = torch.empty((N, I), dtype=tokens.dtype, device=tokens.device)
+    if save and gate_up_save is None:
+        gate_up_save = torch.empty((N, 2 * I), dtype=tokens.dtype, device=tokens.device)
+    _call("moe_gate_up_swiglu_gather", _ptr(tokens), T, _ptr(sorted_indices), K,
+          _ptr(expert_offsets), N, H, I, E, _ptr(W_gate), _ptr(W_up), _ptr(act),
+          _ptr(gate_up_save), _ptr(dev_status), _stream())
+    return act, gate_up_save
+
+
+def moe_gate_up_wgrad_gather(dgu, tokens, sorted_indices, K: int, expert_offsets, *, dW_gate,
+                             dW_up, dev_status=None):
+    """moe_gate_up_wgrad with X = tokens[sorted_indices[i] // K], gathered in
+    the GEMM (bf16)."""
+    _check(tokens, torch.bfloat16, "tokens")
+    _check(sorted_indices, torch.int32, "sorted_indices")
+    T, H = tokens.shape
+    N = dgu.shape[0]
+    E, I, _ = dW_gate.shape
+    _call("moe_gate_up_wgrad_gather", _ptr(dgu), _ptr(tokens), T, _ptr(sorted_indices), K,
+          _ptr(expert_offsets), N, H, I, E, _ptr(dW_gate), _ptr(dW_up), _ptr(dev_status),
+          _stream())
     return dW_gate, dW_up
 
 

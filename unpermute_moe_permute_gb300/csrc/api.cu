@@ -26,6 +26,14 @@ int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, 
 int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
                               int I, int E, void* dWg, void* dWu, int32_t* status,
                               cudaStream_t s);
+int launch_gmm_bf16_gate_up_gather(const void* tokens, int T, const int32_t* sorted_indices, int K,
+                                   const void* Wg, const void* Wu, const int32_t* off, int N, int H,
+                                   int I, int E, void* act, void* save, int32_t* status,
+                                   cudaStream_t s);
+int launch_gate_up_wgrad_bf16_gather(const void* dgu, const void* tokens, int T,
+                                     const int32_t* sorted_indices, int K, const int32_t* off,
+                                     int N, int H, int I, int E, void* dWg, void* dWu,
+                                     int32_t* status, cudaStream_t s);
 
 static std::atomic<unsigned long long> g_launches{0};
 
@@ -199,6 +207,43 @@ extern "C" int moe_gate_up_wgrad(const void* dgu, const void* permuted, int dtyp
     if (int rc = check_ptrs({dgu, permuted})) return rc;
   return launch_gate_up_wgrad_bf16(dgu, permuted, expert_offsets, N, H, I, E, dW_gate, dW_up,
                                    dev_status, stream);
+}
+
+// Arguments of the gathering gate/up calls beyond those of check_mlp.
+static int check_gather(const void* tokens, int T, const int32_t* sorted_indices, int K, int N) {
+  if (K < 1 || K > kMaxK || T < 0) return MOE_ERR_INVALID_ARG;
+  if (N > 0 && (T < 1 || !tokens || !sorted_indices || !aligned16(tokens)))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+extern "C" int moe_gate_up_swiglu_gather(const void* tokens, int T, const int32_t* sorted_indices,
+                                         int K, const int32_t* expert_offsets, int N, int H, int I,
+                                         int E, const void* W_gate, const void* W_up, void* act,
+                                         void* gate_up_save, int32_t* dev_status,
+                                         cudaStream_t stream) {
+  if (int rc = check_mlp(tokens, MOE_BF16, expert_offsets, N, H, I, E)) return rc;
+  if (int rc = check_gather(tokens, T, sorted_indices, K, N)) return rc;
+  if (N == 0) return MOE_OK;
+  if (int rc = check_ptrs({W_gate, W_up, act})) return rc;
+  if (gate_up_save && !aligned16(gate_up_save)) return MOE_ERR_INVALID_ARG;
+  return launch_gmm_bf16_gate_up_gather(tokens, T, sorted_indices, K, W_gate, W_up,
+                                        expert_offsets, N, H, I, E, act, gate_up_save,
+                                        dev_status, stream);
+}
+
+extern "C" int moe_gate_up_wgrad_gather(const void* dgu, const void* tokens, int T,
+                                        const int32_t* sorted_indices, int K,
+                                        const int32_t* expert_offsets, int N, int H, int I, int E,
+                                        void* dW_gate, void* dW_up, int32_t* dev_status,
+                                        cudaStream_t stream) {
+  if (int rc = check_mlp(dgu, MOE_BF16, expert_offsets, N, H, I, E)) return rc;
+  if (int rc = check_gather(tokens, T, sorted_indices, K, N)) return rc;
+  if (int rc = check_ptrs({dW_gate, dW_up})) return rc;
+  if (N > 0)
+    if (int rc = check_ptrs({dgu})) return rc;
+  return launch_gate_up_wgrad_bf16_gather(dgu, tokens, T, sorted_indices, K, expert_offsets, N, H,
+                                          I, E, dW_gate, dW_up, dev_status, stream);
 }
 
 extern "C" int moe_expert_mlp_grad(const void* grad_expanded, const void* permuted,

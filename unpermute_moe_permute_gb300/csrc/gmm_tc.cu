@@ -133,7 +133,29 @@ struct Params {
   __nv_bfloat16* save;
   const __nv_bfloat16* aux;
   int32_t* status;
+  // Permute fused into the load (forward gate/up A rows, gate/up wgrad X
+  // rows): row i of the expert-major operand is row gather[i] / gk of the
+  // [g_rows, g_cols] bf16 token matrix at gsrc.  nullptr: the operand is the
+  // permuted buffer.
+  const int32_t* gather;
+  int gk;
+  int g_rows;
+  int g_cols;
+  const uint8_t* gsrc;
 };
+
+// Stage barriers of a gathering producer: lane 0's arrival (with the byte
+// count of the TMA-loaded operand) and one cp.async arrival per lane.
+constexpr uint32_t kGatherArrivals = 33;
+
+// Token row behind expert-major row i, or row 0 for rows that are never
+// stored or are zeroed (past the expert's end); clamped so that a corrupt
+// index cannot leave the token matrix.
+__device__ __forceinline__ int gather_row(const Params& p, int i, int hi) {
+  if (i >= hi) return 0;
+  const int t = __ldg(p.gather + i) / p.gk;
+  return (t >= 0 && t < p.g_rows) ? t : 0;
+}
 
 struct Tile {
   int e, lo, hi;  // expert and its row range
@@ -513,6 +535,135 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
   }
 }
 
+// Producer warp when the operand rows are gathered from the token matrix:
+// all 32 lanes copy the gathered operand with 16-byte cp.async copies into
+// the 128-byte-swizzled layout the TMA box loads produce (eight lanes per
+// 128-byte row segment, so the reads are coalesced; chunk c of row r lands in
+// chunk c ^ (r & 7)), then arrive on the stage's full barrier when their
+// copies have landed; lane 0 arms the barrier with the byte count of the
+// other operand and loads it with TMA.  Forward gate/up: the 128 A rows of a
+// tile (row indices read once per tile).  Gate/up wgrad: the 64 X rows (k)
+// of a k block in each of the four 64-column B boxes (the next block's row
+// indices read before waiting for its stage).  Single-CTA kinds only.  (A
+// tile::gather4 TMA form of the same loads was correct but measured 2.4x
+// slower for the forward and 5x for the wgrad on GB300: it moves 512 bytes
+// per instruction and the TMA unit takes ~40 ns per gather.)
+template <int KIND>
+__device__ __forceinline__ void produce_gathered(const Params& p, const int32_t* prefix,
+                                                 const int32_t* offs, int total, int t_first,
+                                                 int t_step, int lane, uint32_t sA, uint32_t sB,
+                                                 uint32_t ctrl, volatile int* abort_flag,
+                                                 const CUtensorMap* mA, const CUtensorMap* mB0,
+                                                 const CUtensorMap* mB1) {
+  constexpr int STAGES = Traits<KIND>::stages;
+  constexpr uint32_t A_BYTES = Traits<KIND>::a_bytes;
+  constexpr uint32_t B_BYTES = Traits<KIND>::b_bytes;
+  constexpr uint32_t MN_BOX_BYTES = Traits<KIND>::mn_box;
+  constexpr int BK = Traits<KIND>::bk;
+  static_assert(!Traits<KIND>::pair, "gathered operands are single-CTA");
+  auto full_bar = [&](int s) { return ctrl + 8u * s; };
+  auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
+  auto tail_bar = [&](int s) { return ctrl + 8u * (3 * STAGES + 5 + s); };
+  const int c = lane & 7, r0 = lane >> 3;  // 16-byte chunk and first row of this lane
+  const size_t ld = (size_t)p.g_cols * 2;  // token row bytes
+  auto swz = [&](int row) { return (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4); };
+  int issued[kMaxStages];
+#pragma unroll
+  for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+  int g = 0;
+  bool run = true;
+  if constexpr (kind_of(KIND) == kFwdGateUp) {
+    for (int t = t_first; run && t < total; t += t_step) {
+      const Tile x = decode_tile<KIND>(t, p, prefix, offs, 0);
+      int tok[BM / 4];  // token rows of tile rows r0 + 4j
+#pragma unroll
+      for (int j = 0; j < BM / 4; ++j) tok[j] = gather_row(p, x.m0 + r0 + 4 * j, x.hi);
+      for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status))) {
+          run = false;
+          break;
+        }
+        const int k0 = kb * BK;
+        const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(s), B_BYTES);
+          tma_load_3d(sb, mB0, full_bar(s), k0, x.n0, x.e);
+          tma_load_3d(sb + B_BYTES / 2, mB1, full_bar(s), k0, x.n0, x.e);
+          issued[s] = (int)ph;
+        }
+        const uint8_t* col = p.gsrc + (size_t)k0 * 2 + (size_t)c * 16;
+#pragma unroll
+        for (int j = 0; j < BM / 4; ++j) cp_async_16(sa + swz(r0 + 4 * j), col + (size_t)tok[j] * ld, 16);
+        cp_async_arrive(full_bar(s));
+      }
+    }
+  } else {
+    static_assert(kind_of(KIND) == kWgradGateUp, "gathers serve the gate/up GEMMs");
+    // the (tile, k block) position the producer fills next, skipping tiles
+    // without rows (they have no k blocks)
+    int t = t_first, kb = 0;
+    Tile x{};
+    auto next_tile = [&]() {
+      for (; t < total; t += t_step) {
+        x = decode_tile<KIND>(t, p, prefix, offs, 0);
+        if (x.kblocks > 0) return true;
+      }
+      return false;
+    };
+    bool have = next_tile();
+    int tok[BK / 4];  // token rows of k rows r0 + 4j of the block
+    auto load_rows = [&]() {
+      const int base = x.lo + kb * BK + r0;
+#pragma unroll
+      for (int j = 0; j < BK / 4; ++j) tok[j] = gather_row(p, base + 4 * j, x.hi);
+    };
+    if (have) load_rows();
+    while (have) {
+      const int s = g % STAGES;
+      const uint32_t ph = (g / STAGES) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status))) break;
+      const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
+      const int row = x.lo + kb * BK;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full_bar(s), A_BYTES);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * MN_BOX_BYTES, mA, full_bar(s), x.m0 + j * 64, row);
+        issued[s] = (int)ph;
+        if (k_tail<KIND>(x, kb).zl > 0) mbar_arrive(tail_bar(s));
+      }
+#pragma unroll
+      for (int box = 0; box < Traits<KIND>::b_rows / 64; ++box) {
+        const int colx = x.n0 + box * 64 + c * 8;  // columns past H are zero-filled
+        const uint32_t bytes = colx < p.g_cols ? 16u : 0u;
+        const uint8_t* col = p.gsrc + (bytes ? (size_t)colx * 2 : 0);
+#pragma unroll
+        for (int j = 0; j < BK / 4; ++j)
+          cp_async_16(sb + box * MN_BOX_BYTES + swz(r0 + 4 * j), col + (bytes ? (size_t)tok[j] * ld : 0),
+                      bytes);
+      }
+      cp_async_arrive(full_bar(s));
+      ++g;
+      if (++kb == x.kblocks) {
+        kb = 0;
+        t += t_step;
+        have = next_tile();
+      }
+      if (have) load_rows();  // in flight while the next stage is awaited
+    }
+  }
+  // wait for every copy issued before the CTA may exit (the full barriers
+  // count the lanes' cp.async arrivals too)
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s)
+      if (issued[s] >= 0) mbar_wait(full_bar(s), (uint32_t)issued[s], abort_flag, p.status, false);
+  }
+  __syncwarp();
+  (void)mA;
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(Traits<KIND>::threads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
@@ -552,13 +703,17 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   int32_t* scratch = offs + (kMaxExperts + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // operand rows gathered from the token matrix by the producer's cp.async
+  bool gathered = false;
+  if constexpr ((kind_of(KIND) == kFwdGateUp || kind_of(KIND) == kWgradGateUp) && !PAIR)
+    gathered = p.gather != nullptr;
   if (threadIdx.x == 0) {
     // In a pair the leader's full barriers count both CTAs' bytes, the
     // leader's MMA commits release the stages and accumulators of both CTAs,
     // and the leader's tempty barriers take one arrival per epilogue warp of
     // both CTAs.
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), gathered ? kGatherArrivals : 1u);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -615,7 +770,12 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
+    if constexpr ((kind_of(KIND) == kFwdGateUp || kind_of(KIND) == kWgradGateUp) && !PAIR) {
+      if (gathered)
+        produce_gathered<KIND>(p, prefix, offs, total, t_first, t_step, lane, sA, sB, ctrl,
+                               abort_flag, &mapA, &mapB0, &mapB1);
+    }
+    if (!gathered && lane == 0) {
       int issued[kMaxStages];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) issued[s] = -1;
@@ -698,6 +858,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             tc_fence_after();
           }
         }
+        // operand rows written by the producer's cp.async (generic proxy),
+        // now visible to this thread, made visible to the MMA's reads
+        if (gathered) fence_proxy_async_smem();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
@@ -944,13 +1107,15 @@ bool store_map_3d(CUtensorMap* m, const void* ptr, int cols, int rows, int E) {
   return make_map(m, ptr, 3, d, b, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const int32_t* off,
-                            int N, int H, int I, int E, void* act, void* save, int32_t* status,
-                            cudaStream_t s) {
+// Forward gate/up.  gather == nullptr: A is the permuted [N, H] buffer;
+// otherwise A row i is row gather[i] / K of the token matrix A [T, H].
+static int gate_up_bf16(const void* A, int T, const int32_t* gather, int K, const void* Wg,
+                        const void* Wu, const int32_t* off, int N, int H, int I, int E, void* act,
+                        void* save, int32_t* status, cudaStream_t s) {
   if (int rc = device_ok()) return rc;
   CUtensorMap ma, mg, mu;
-  const uint64_t da[2] = {(uint64_t)H, (uint64_t)N};
-  const uint32_t ba[2] = {64, 128};
+  const uint64_t da[2] = {(uint64_t)H, (uint64_t)(gather ? T : N)};
+  const uint32_t ba[2] = {64, gather ? 1u : 128u};  // (not read when gathering)
   const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)E};
   const uint32_t bw[3] = {64, 128, 1};
   if (!make_map(&ma, A, 2, da, ba) || !make_map(&mg, Wg, 3, dw, bw) || !make_map(&mu, Wu, 3, dw, bw))
@@ -962,12 +1127,31 @@ int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const
   p.n_tiles = (I + 127) / 128;
   p.out = static_cast<__nv_bfloat16*>(act);
   p.save = static_cast<__nv_bfloat16*>(save);
+  p.gather = gather;
+  p.gk = K;
+  p.g_rows = T;
+  p.g_cols = H;
+  p.gsrc = static_cast<const uint8_t*>(A);
   CUtensorMap c_act, c_save;
   if (!store_map_2d(&c_act, act, I, N) || !store_map_2d(&c_save, save ? save : act, save ? 2 * I : I, N))
     return MOE_ERR_CUDA;
-  return use_pairs(kPairMinRowsGateUp, N, E)
+  // gathered A rows are loaded by the single-CTA producer only
+  return (gather == nullptr && use_pairs(kPairMinRowsGateUp, N, E))
              ? launch<kFwdGateUp | kPaired>(ma, mg, mu, c_act, c_save, p, s)
              : launch<kFwdGateUp>(ma, mg, mu, c_act, c_save, p, s);
+}
+
+int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const int32_t* off,
+                            int N, int H, int I, int E, void* act, void* save, int32_t* status,
+                            cudaStream_t s) {
+  return gate_up_bf16(A, N, nullptr, 1, Wg, Wu, off, N, H, I, E, act, save, status, s);
+}
+
+int launch_gmm_bf16_gate_up_gather(const void* tokens, int T, const int32_t* sorted_indices, int K,
+                                   const void* Wg, const void* Wu, const int32_t* off, int N, int H,
+                                   int I, int E, void* act, void* save, int32_t* status,
+                                   cudaStream_t s) {
+  return gate_up_bf16(tokens, T, sorted_indices, K, Wg, Wu, off, N, H, I, E, act, save, status, s);
 }
 
 int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int N, int H, int I,
@@ -1066,17 +1250,22 @@ int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, 
   return launch<kWgradDown>(m_a, m_b, m_b, c_dwd, c_dwd, p, s);
 }
 
-int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
-                              int I, int E, void* dWg, void* dWu, int32_t* status,
-                              cudaStream_t s) {
+// Gate/up wgrad.  gather == nullptr: X is the permuted [N, H] buffer;
+// otherwise X row i is row gather[i] / K of the token matrix X [T, H].
+static int gate_up_wgrad_bf16(const void* dgu, const void* X, int T, const int32_t* gather, int K,
+                              const int32_t* off, int N, int H, int I, int E, void* dWg,
+                              void* dWu, int32_t* status, cudaStream_t s) {
   if (int rc = device_ok()) return rc;
   const uint32_t box_mn2[2] = {64, (uint32_t)Traits<kWgradGateUp>::bk};
+  const uint32_t box_row[2] = {64, 1};  // (not read when gathering)
   CUtensorMap m_a, m_b;
   const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
+  const uint64_t x_rows = gather ? (uint64_t)(T > 0 ? T : 1) : rows;
   const uint64_t d_a[2] = {(uint64_t)2 * I, rows};
-  const uint64_t d_b[2] = {(uint64_t)H, rows};
-  if (!make_map(&m_a, N > 0 ? dgu : dWg, 2, d_a, box_mn2) ||
-      !make_map(&m_b, N > 0 ? X : dWg, 2, d_b, box_mn2))
+  const uint64_t d_b[2] = {(uint64_t)H, x_rows};
+  const bool any = N > 0 && (gather == nullptr || T > 0);
+  if (!make_map(&m_a, any ? dgu : dWg, 2, d_a, box_mn2) ||
+      !make_map(&m_b, any ? X : dWg, 2, d_b, gather ? box_row : box_mn2))
     return MOE_ERR_CUDA;
   Params p = base_params(off, N, E, status);
   p.I = I;
@@ -1086,10 +1275,29 @@ int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off
   p.n_tiles = (H + 255) / 256;
   p.out = static_cast<__nv_bfloat16*>(dWg);
   p.out2 = static_cast<__nv_bfloat16*>(dWu);
+  p.gather = gather;
+  p.gk = K;
+  p.g_rows = T;
+  p.g_cols = H;
+  p.gsrc = static_cast<const uint8_t*>(X);
   CUtensorMap c_dwg, c_dwu;
   if (!store_map_3d(&c_dwg, dWg, H, I, E) || !store_map_3d(&c_dwu, dWu, H, I, E))
     return MOE_ERR_CUDA;
   return launch<kWgradGateUp>(m_a, m_b, m_b, c_dwg, c_dwu, p, s);
+}
+
+int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
+                              int I, int E, void* dWg, void* dWu, int32_t* status,
+                              cudaStream_t s) {
+  return gate_up_wgrad_bf16(dgu, X, N, nullptr, 1, off, N, H, I, E, dWg, dWu, status, s);
+}
+
+int launch_gate_up_wgrad_bf16_gather(const void* dgu, const void* tokens, int T,
+                                     const int32_t* sorted_indices, int K, const int32_t* off,
+                                     int N, int H, int I, int E, void* dWg, void* dWu,
+                                     int32_t* status, cudaStream_t s) {
+  return gate_up_wgrad_bf16(dgu, tokens, T, sorted_indices, K, off, N, H, I, E, dWg, dWu, status,
+                            s);
 }
 
 }  // namespace moe
