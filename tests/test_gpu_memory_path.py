@@ -209,6 +209,8 @@ def test_invert_sorted_indices(lib):
     (500, 8, 64, 264, 4, 4, 4, True),
     (200, 8, 32, 128, 0, 0, 0, False),
     (64, 2, 4, 64, 2, 0, 3, False),
+    (300, 8, 32, 520, 2, 2, 2, True),     # 65 column vectors: a ragged last lane pass
+    (5000, 4, 16, 520, 1, 1, 1, True),    # 625 blocks of 8 tokens
 ])
 def test_combine(lib, T, K, E, H, Z, C, Cn, shared):
     d = moe_inputs.index_combine(T + H, R=1, E_local=E, T=T, H=H, K=K, zero_num=Z, copy_num=C,
