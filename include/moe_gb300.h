@@ -84,6 +84,15 @@ int moe_abi_version(void);
  * devices, all streams).  For tracing and launch accounting. */
 unsigned long long moe_kernel_launches(void);
 
+/* Self-test of the bounded waits that every tensor-core kernel here relies
+ * on.  The paper has no counterpart; it lets a deployment exercise the
+ * failure path without faulting or hanging a GPU.  One thread waits, with
+ * the same bounded mbarrier wait the GEMMs use, on a barrier that nothing
+ * arrives on; after the wait limit (2 s) it records MOE_ERR_TIMEOUT in
+ * dev_status (required, device int32, initialise to 0) and returns, so the
+ * context stays usable.  Returns MOE_ERR_INVALID_ARG for a NULL dev_status. */
+int moe_selftest_bounded_wait(int32_t* dev_status, cudaStream_t stream);
+
 /* Synchronise `stream`, then read the device status word written by earlier
  * calls.  Returns MOE_OK or the first device-side MOE_ERR_* code, or
  * MOE_ERR_CUDA if the stream reported an error.  Does not reset the word. */

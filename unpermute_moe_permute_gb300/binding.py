@@ -78,6 +78,7 @@ _SIGNATURES = {
     "moe_gate_up_dgrad": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_down_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_gate_up_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_selftest_bounded_wait": ([_P, _P], _I),
     "moe_gate_up_swiglu_gather": ([_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_gate_up_wgrad_gather": ([_P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
 }
@@ -148,6 +149,12 @@ def _check(t: Optional[torch.Tensor], dtype, name: str):
 def new_status(device=None) -> torch.Tensor:
     """A zeroed device status word for the dev_status arguments."""
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def moe_selftest_bounded_wait(dev_status) -> None:
+    """Run the bounded-wait self-test (about 2 s on the GPU): dev_status
+    receives MOE_ERR_TIMEOUT."""
+    _call("moe_selftest_bounded_wait", _ptr(dev_status), _stream())
 
 
 def moe_kernel_launches() -> int:

@@ -26,6 +26,7 @@ int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, 
 int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
                               int I, int E, void* dWg, void* dWu, int32_t* status,
                               cudaStream_t s);
+int launch_wait_selftest(int32_t* status, cudaStream_t s);
 int launch_gmm_bf16_gate_up_gather(const void* tokens, int T, const int32_t* sorted_indices, int K,
                                    const void* Wg, const void* Wu, const int32_t* off, int N, int H,
                                    int I, int E, void* act, void* save, int32_t* status,
@@ -88,6 +89,11 @@ extern "C" int moe_abi_version(void) { return 1; }
 
 extern "C" unsigned long long moe_kernel_launches(void) {
   return g_launches.load(std::memory_order_relaxed);
+}
+
+extern "C" int moe_selftest_bounded_wait(int32_t* dev_status, cudaStream_t stream) {
+  if (dev_status == nullptr) return MOE_ERR_INVALID_ARG;
+  return launch_wait_selftest(dev_status, stream);
 }
 
 extern "C" int moe_check_status(const int32_t* dev_status, cudaStream_t stream) {

@@ -967,6 +967,19 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   }
 }
 
+// A bounded wait that runs out: nothing arrives on the barrier.
+__global__ void wait_selftest_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, status);
+}
+
 // ---- host side -----------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1290,6 +1303,12 @@ int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off
                               int I, int E, void* dWg, void* dWu, int32_t* status,
                               cudaStream_t s) {
   return gate_up_wgrad_bf16(dgu, X, N, nullptr, 1, off, N, H, I, E, dWg, dWu, status, s);
+}
+
+int launch_wait_selftest(int32_t* status, cudaStream_t s) {
+  tc::wait_selftest_kernel<<<1, 32, 0, s>>>(status);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int launch_gate_up_wgrad_bf16_gather(const void* dgu, const void* tokens, int T,
