@@ -484,6 +484,84 @@ class LayerForward(LayerFwdBwd):
         super().__init__(lib, dev, seed, gen=moe_inputs.layer_forward_zipf, backward=False, **kw)
 
 
+class SharedExpertOverlap:
+    """T=4096 H=2048 E=128 K=8 I=768 bf16 forward plus a shared expert
+    (I=1536) whose output the combine adds: one stream, or the shared expert
+    on a second stream concurrently with the routed path."""
+
+    name = "shared_expert_overlap"
+
+    def __init__(self, lib, dev, seed=0, I_shared=1536):
+        d = moe_inputs.layer_fwd_bwd(seed)
+        s = moe_inputs.layer_fwd_bwd(seed + 1, T=1, H=d["H"], E=1, K=1, I=I_shared)
+        self.lib, self.dev = lib, dev
+        T, H, E, K, I = d["T"], d["H"], d["E"], d["K"], d["I"]
+        self.T, self.E, self.K = T, E, K
+        self.x = {k: d[k].to(dev) for k in ("tokens", "expert_ids", "probs")}
+        self.Wg, self.Wu, self.Wd = d["W_gate"].to(dev), d["W_up"].to(dev), d["W_down"].to(dev)
+        self.Sg, self.Su, self.Sd = (s["W_gate"][0].to(dev), s["W_up"][0].to(dev),
+                                     s["W_down"][0].to(dev))
+        N, bf = T * K, torch.bfloat16
+        e = lambda *shape, dt=bf: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+        self.permuted, self.sorted, self.row_map = e(N, H), e(N, dt=torch.int32), e(N, dt=torch.int32)
+        self.tpe, self.off = e(E, dt=torch.int32), e(E + 1, dt=torch.int32)
+        self.ws = e(max(lib.moe_permute_workspace_size(T, K, E), 16), dt=torch.uint8)
+        self.act, self.expanded, self.out = e(N, I), e(N, H), e(T, H)
+        self.s_act, self.shared = e(T, I_shared), e(T, H)
+        self.side = torch.cuda.Stream(device=dev)
+        self.config = {"workload": f"layer forward T={T} H={H} E={E} K={K} I={I} plus a shared "
+                                   f"expert I={I_shared}, bf16"}
+
+    def _shared(self):
+        self.lib.moe_shared_expert_mlp(self.x["tokens"], self.Sg, self.Su, self.Sd,
+                                       act=self.s_act, out=self.shared)
+
+    def _routed(self):
+        lib, x = self.lib, self.x
+        lib.moe_permute(x["tokens"], x["expert_ids"], self.E, 0, permuted=self.permuted,
+                        sorted_indices=self.sorted, row_map=self.row_map,
+                        tokens_per_expert=self.tpe, expert_offsets=self.off, workspace=self.ws)
+        lib.moe_gate_up_swiglu(self.permuted, self.off, self.Wg, self.Wu, act=self.act)
+        lib.moe_down_proj(self.act, self.off, self.Wd, expanded=self.expanded)
+
+    def _combine(self):
+        x = self.x
+        self.lib.moe_combine(self.expanded, self.row_map, x["expert_ids"], x["probs"], self.E,
+                             shared_x=self.shared, out=self.out)
+
+    def step(self, overlapped: bool):
+        main = torch.cuda.current_stream(self.dev)
+        if not overlapped:
+            self._shared()
+            self._routed()
+        else:
+            ready = torch.cuda.Event()
+            ready.record(main)
+            with torch.cuda.stream(self.side):
+                self.side.wait_event(ready)
+                self._shared()
+                done = torch.cuda.Event()
+                done.record(self.side)
+            self._routed()
+            main.wait_event(done)
+        self._combine()
+
+    def measure(self, steps=20, warmup=3):
+        res = {}
+        for overlapped in (False, True):
+            for _ in range(warmup):
+                self.step(overlapped)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                self.step(overlapped)
+            b.record()
+            torch.cuda.synchronize()
+            res["overlapped_us" if overlapped else "one_stream_us"] = a.elapsed_time(b) / steps * 1e3
+        return res
+
+
 class IndexCombine:
     """Permute-index generation from counts[16 x 16] and the combine of
     T=4096 H=7168 K=8 over 256 real + 4 zero + 4 copy + 4 const experts."""
@@ -583,6 +661,10 @@ def run_components(lib, dev, peaks, steps=10, warmup=3):
             "kernels": kernel_table(per, w, peaks)}
         del w
         torch.cuda.empty_cache()
+    w = SharedExpertOverlap(lib, dev)
+    comps[w.name] = {"config": w.config["workload"], "forward_us": w.measure()}
+    del w
+    torch.cuda.empty_cache()
     return comps
 
 

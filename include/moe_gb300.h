@@ -212,6 +212,24 @@ int moe_expert_mlp(const void* permuted, int dtype, const int32_t* expert_offset
                    void* act, void* expanded, void* gate_up_save, int32_t* dev_status,
                    cudaStream_t stream);
 
+/* ---- shared expert (torch_npu npu_moe_distribute_combine_v2 API reference,
+ * shared_expert_x: the value added after the combine; hyper_parallel
+ * expert_parallel.py, combine_start: the combine split so that a shared
+ * expert forward can run meanwhile) ---------------------------------------
+ *
+ * The shared expert's MLP over every token, on the caller's stream:
+ *   act = silu(x W_gate^T) * (x W_up^T),   out = act W_down^T
+ * x [T, H] bf16, W_gate and W_up [I, H], W_down [H, I] bf16, act [T, I] and
+ * out [T, H] bf16 (caller-owned).  The same tcgen05 kernels as the routed
+ * experts, as one expert that owns all T rows.  Run it on a second stream,
+ * concurrently with the routed path, and pass out as moe_combine's
+ * shared_x after the stream join (an event); moe_combine adds it.
+ * H and I multiples of 64; returns MOE_ERR_SHAPE otherwise.
+ */
+int moe_shared_expert_mlp(const void* x, int T, int H, int I, const void* W_gate,
+                          const void* W_up, const void* W_down, void* act, void* out,
+                          int32_t* dev_status, cudaStream_t stream);
+
 /* ---- the permute fused into the gate/up GEMMs (bf16) --------------------
  *
  * The twinkle PR "NPU EP experts forward uses NPU grouped matmul" feeds the

@@ -79,6 +79,7 @@ _SIGNATURES = {
     "moe_down_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_gate_up_wgrad": ([_P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_selftest_bounded_wait": ([_P, _P], _I),
+    "moe_shared_expert_mlp": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_gate_up_swiglu_gather": ([_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_gate_up_wgrad_gather": ([_P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
 }
@@ -371,6 +372,21 @@ def moe_gate_up_wgrad(dgu, permuted, expert_offsets, *, dW_gate, dW_up, dev_stat
     _call("moe_gate_up_wgrad", _ptr(dgu), _ptr(permuted), _dtype(permuted), _ptr(expert_offsets),
           N, H, I, E, _ptr(dW_gate), _ptr(dW_up), _ptr(dev_status), _stream())
     return dW_gate, dW_up
+
+
+def moe_shared_expert_mlp(x, W_gate, W_up, W_down, *, act=None, out=None, dev_status=None):
+    """Shared-expert MLP over all tokens (bf16): out = (silu(x Wg^T) * x Wu^T) Wd^T.
+    Runs on the current stream; pass out as moe_combine's shared_x."""
+    _check(x, torch.bfloat16, "x")
+    T, H = x.shape
+    I = W_gate.shape[0]
+    if act is None:
+        act = torch.empty((T, I), dtype=x.dtype, device=x.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    _call("moe_shared_expert_mlp", _ptr(x), T, H, I, _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+          _ptr(act), _ptr(out), _ptr(dev_status), _stream())
+    return out
 
 
 def moe_gate_up_swiglu_gather(tokens, sorted_indices, K: int, expert_offsets, W_gate, W_up, *,

@@ -215,6 +215,21 @@ extern "C" int moe_gate_up_wgrad(const void* dgu, const void* permuted, int dtyp
                                    dev_status, stream);
 }
 
+extern "C" int moe_shared_expert_mlp(const void* x, int T, int H, int I, const void* W_gate,
+                                     const void* W_up, const void* W_down, void* act, void* out,
+                                     int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 64 || I % 64) return MOE_ERR_SHAPE;
+  if ((long long)T * (2LL * I > H ? 2LL * I : H) > (1LL << 40)) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (int rc = check_ptrs({x, W_gate, W_up, W_down, act, out})) return rc;
+  // one expert owning all T rows (no offsets array: the kernels imply [0, T])
+  if (int rc = launch_gmm_bf16_gate_up(x, W_gate, W_up, nullptr, T, H, I, 1, act, nullptr,
+                                       dev_status, stream))
+    return rc;
+  return launch_gmm_bf16_down(act, W_down, nullptr, T, H, I, 1, out, dev_status, stream);
+}
+
 // Arguments of the gathering gate/up calls beyond those of check_mlp.
 static int check_gather(const void* tokens, int T, const int32_t* sorted_indices, int K, int N) {
   if (K < 1 || K > kMaxK || T < 0) return MOE_ERR_INVALID_ARG;

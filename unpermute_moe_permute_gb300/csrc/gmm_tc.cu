@@ -119,7 +119,7 @@ struct Traits {
 };
 
 struct Params {
-  const int32_t* off;
+  const int32_t* off;  // expert row offsets [E+1]; nullptr: one expert owning all N rows
   int N;        // row capacity of the token-major buffers
   int E;
   int Kd;       // reduction length of the row-tiled kinds
@@ -748,7 +748,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   }
   // Every role decodes every tile; the offsets are read from global memory
   // once here instead of once per tile and role.
-  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) offs[e] = p.off[e];
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x)
+    offs[e] = p.off != nullptr ? p.off[e] : (e == 0 ? 0 : p.N);
   __syncthreads();
   int total;
   if constexpr (Traits<KIND>::wgrad) {
