@@ -31,7 +31,10 @@ def _oracle_shared(x, Wg, Wu, Wd):
     return act, out
 
 
-@pytest.mark.parametrize("T,H,I", [(700, 256, 192), (1, 64, 64), (300, 320, 128)])
+@pytest.mark.parametrize("T,H,I", [
+    (700, 256, 192), (1, 64, 64), (300, 320, 128),
+    (1100, 256, 192),     # paired: four full pair tiles and a half tile
+])
 def test_shared_expert_mlp(lib, T, H, I):
     x = moe_inputs.layer_fwd_bwd(T + I, T=T, H=H, E=1, K=1, I=64)["tokens"]
     Wg, Wu, Wd = _shared_weights(T + H, H, I)

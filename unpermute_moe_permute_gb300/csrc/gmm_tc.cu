@@ -87,17 +87,20 @@ struct Traits {
   // adjacent 128-row tiles of one expert and n tile and hold half of the
   // B tile each, so per SM the MMA reads and the TMA writes 32 KB of shared
   // memory per k block instead of 48 KB, which leaves room for a 6-stage
-  // ring.  The price is a wasted half tile for every expert with an odd
-  // number of 128-row tiles, so whether a call runs paired is decided per
-  // call from the rows per expert (use_pairs).  The dgrads measured no
-  // better paired at the layer shapes, and the wgrads stay single: their
-  // expert tail rows are zeroed in shared memory after the loads land,
-  // which the leader cannot observe for the peer's loads.
+  // ring.  When at most 128 of an expert's rows are left, the pair takes
+  // them as a half tile (M=128 over the pair, 64 rows per CTA), so pairs
+  // cover the same rows as single CTAs.  Whether a call runs paired
+  // is decided per call and kind from the rows per expert (use_pairs).  The
+  // wgrads stay single: their expert tail rows are zeroed in shared memory
+  // after the loads land, which the leader cannot observe for the peer's
+  // loads.
   static constexpr bool pair = (KIND & kPaired) != 0;
   static_assert(!(pair && wgrad), "the wgrad tail fix-up is single-CTA");
   static constexpr int cs = pair ? 2 : 1;  // CTAs per cluster
   static constexpr int b_rows = pair ? bn / 2 : bn;  // B rows (N) this CTA holds
   static constexpr uint32_t idesc = idesc_bf16_f32(BM * cs, bn, a_mn, b_mn);
+  // a pair's half tile: M=128 over the pair, 64 A rows per CTA
+  static constexpr uint32_t idesc_half = idesc_bf16_f32(BM, bn, a_mn, b_mn);
   // k-block depth and ring depth: 64-deep blocks (one 128-byte swizzle row)
   // in 4 stages for every kind.  Measured on GB300: a fourth stage beats a
   // second staging unit per epilogue warp, and for the wgrads 32-deep blocks
@@ -107,7 +110,8 @@ struct Traits {
   // The SwiGLU-backward epilogue stages two units (dg, du) per piece and is
   // the slower side of its kernel: it trades a stage for a two-unit ring.
   static constexpr int nbuf = kind_of(KIND) == kDgradDown ? 2 : 1;
-  static constexpr int stages = pair ? (kind_of(KIND) == kDgradDown ? 5 : 6) : (kind_of(KIND) == kDgradDown ? 3 : 4);
+  static constexpr int stages = pair ? 6 : (kind_of(KIND) == kDgradDown ? 3 : 4);
+  static_assert(!(pair && kind_of(KIND) == kDgradDown), "the down dgrad runs single-CTA");
   static constexpr uint32_t a_bytes = BM * bk * 2;
   static constexpr uint32_t b_bytes = b_rows * bk * 2;
   static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
@@ -161,6 +165,7 @@ struct Tile {
   int e, lo, hi;  // expert and its row range
   int m0, n0;     // first output row / column of the tile
   int kblocks;    // 64-deep k blocks
+  int rows;       // A rows this CTA owns: 128, or 64 in a pair's half tile
 };
 
 // Wgrad k block kb of tile x (k = the expert's token rows): the MMAs cover
@@ -185,8 +190,11 @@ __device__ __forceinline__ KTail k_tail(const Tile& x, int kb) {
 
 // Tile t: a group of CS (1, or 2 for a pair) vertically adjacent 128-row tiles of one
 // expert and one n tile; this CTA (cluster rank `rank`) takes the rank-th.
-// A rank whose rows lie past the expert's end computes a tile that is never
-// stored (its loads read the next expert's rows, or zeros past the buffer).
+// When at most 128 rows of the expert are left, a pair takes them as a half
+// tile (M=128 over the pair, 64 rows per CTA), so that pairs cover exactly
+// the rows single CTAs would.  Rows past the expert's end are computed and
+// never stored (their loads read the next expert's rows, or zeros past the
+// buffer).
 template <int KIND>
 __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_t* prefix,
                                             const int32_t* offs, int rank) {
@@ -199,7 +207,9 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.e = e;
     x.lo = r.lo;
     x.hi = r.hi;
-    x.m0 = r.lo + (mg - prefix[e]) * (BM * CS) + rank * BM;
+    const int g0 = r.lo + (mg - prefix[e]) * (BM * CS);  // first row of the (pair) tile
+    x.rows = (CS == 2 && g0 + BM >= r.hi) ? BM / 2 : BM;
+    x.m0 = g0 + rank * x.rows;
     x.n0 = nt * Traits<KIND>::n_per_tile;
     x.kblocks = p.Kd / Traits<KIND>::bk;
   } else {
@@ -212,6 +222,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.lo = r.lo;
     x.hi = r.hi;
     x.m0 = (mg * CS + rank) * BM;
+    x.rows = BM;
     x.n0 = nt * Traits<KIND>::bn;
     x.kblocks = (r.hi - r.lo + Traits<KIND>::bk - 1) / Traits<KIND>::bk;
   }
@@ -225,8 +236,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
 template <int KIND>
 __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& p, uint32_t sa,
                                            uint32_t sb, uint32_t bar, const CUtensorMap* mA,
-                                           const CUtensorMap* mB0, const CUtensorMap* mB1,
-                                           int rank, bool load_a) {
+                                           const CUtensorMap* mA64, const CUtensorMap* mB0,
+                                           const CUtensorMap* mB1, int rank, bool load_a) {
   constexpr bool PAIR = Traits<KIND>::pair;
   constexpr int B_ROWS = Traits<KIND>::b_rows;
   constexpr uint32_t MN_BOX_BYTES = Traits<KIND>::mn_box;
@@ -240,24 +251,29 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
     else tma_load_3d(dst, m, bar, bx, by, bz);
   };
   const int nb = x.n0 + (PAIR ? rank * B_ROWS : 0);  // first B row (N) of this CTA's part
+  // a pair's half tile needs only its 64 A rows
+  const CUtensorMap* mAr = (PAIR && x.rows < BM) ? mA64 : mA;
   if constexpr (kind_of(KIND) == kFwdGateUp) {
-    // B tile = 128 rows of W_gate, then the same 128 rows of W_up
-    if (load_a) l2(sa, mA, k0, x.m0);
+    // B tile = 128 rows of W_gate, then the same 128 rows of W_up; in a pair
+    // each CTA holds 64 gate rows then the same 64 up rows (its N half), so
+    // that gate and up of one output column meet in one thread
+    if (load_a) l2(sa, mAr, k0, x.m0);
     if constexpr (PAIR) {
-      l3(sb, rank == 0 ? mB0 : mB1, k0, x.n0, x.e);
+      l3(sb, mB0, k0, x.n0 + 64 * rank, x.e);
+      l3(sb + Traits<KIND>::b_bytes / 2, mB1, k0, x.n0 + 64 * rank, x.e);
     } else {
       l3(sb, mB0, k0, x.n0, x.e);
       l3(sb + Traits<KIND>::b_bytes / 2, mB1, k0, x.n0, x.e);
     }
   } else if constexpr (kind_of(KIND) == kFwdDown) {
-    if (load_a) l2(sa, mA, k0, x.m0);
+    if (load_a) l2(sa, mAr, k0, x.m0);
     l3(sb, mB0, k0, nb, x.e);  // B_ROWS rows of the W_down panel in one box
   } else if constexpr (kind_of(KIND) == kDgradDown) {
-    if (load_a) l2(sa, mA, k0, x.m0);
+    if (load_a) l2(sa, mAr, k0, x.m0);
 #pragma unroll
     for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, k0, x.e);
   } else if constexpr (kind_of(KIND) == kDgradGateUp) {
-    if (load_a) l2(sa, mA, k0, x.m0);
+    if (load_a) l2(sa, mAr, k0, x.m0);
     const bool up = k0 >= p.I;
     const int kk = up ? k0 - p.I : k0;
 #pragma unroll
@@ -373,20 +389,45 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
                                          const CUtensorMap* mC0,
                                          const CUtensorMap* mC1) {
   if constexpr (!Traits<KIND>::wgrad) {
-    const int r0 = x.m0 + quarter * 32;
-    if (r0 >= x.hi) return;  // warp-uniform: no row of this quarter is valid
+    // The 32 x 32 pieces this warp drains: piece i covers accumulator rows
+    // r0.. (the warp's TMEM lane quarter), TMEM columns tc0 + 32i and output
+    // columns col0 + 32i.  Single CTAs and full pair tiles hold rows 32q in
+    // lane quarter q with all N columns in TMEM columns 0..N-1; a pair's half
+    // tile holds the CTA's 64 rows in lanes 0-63 for the first N/2 columns
+    // and again in lanes 64-127 for the last N/2, in TMEM columns 0..N/2-1.
+    // Gate/up accumulators hold [gate 128 | up 128] in a single CTA and, in
+    // a pair, [gate 64 | up 64] per CTA half of N (the pair's B halves
+    // interleave gate and up rows), so the up column is tc + uoff.
+    constexpr bool PAIR = Traits<KIND>::pair;
+    const bool halft = PAIR && x.rows < BM;
+    const int r0 = x.m0 + (halft ? 32 * (quarter & 1) : 32 * quarter);
+    const int blk = halft ? (quarter >> 1) : 0;  // which half of N (half tiles)
+    int np, tc0, col0, uoff = 0;
+    if constexpr (kind_of(KIND) == kFwdGateUp) {
+      if (!PAIR) {
+        np = 2, tc0 = 64 * half, uoff = 128, col0 = x.n0 + 64 * half;
+      } else if (!halft) {
+        np = 2, tc0 = 128 * half, uoff = 64, col0 = x.n0 + 64 * half;
+      } else {
+        np = 1, tc0 = 32 * half, uoff = 64, col0 = x.n0 + 64 * blk + 32 * half;
+      }
+    } else {
+      if (!halft) np = 4, tc0 = 128 * half, col0 = x.n0 + 128 * half;
+      else np = 2, tc0 = 64 * half, col0 = x.n0 + 128 * blk + 64 * half;
+    }
+    if (r0 >= x.hi) return;  // warp-uniform: no row of this warp is valid
     const bool full = r0 + 32 <= x.hi;
     const int row = r0 + lane;
     const bool rv = row < x.hi;
     if constexpr (kind_of(KIND) == kFwdGateUp) {
       const int I = p.Nout;
 #pragma unroll 1
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
-        const int col = x.n0 + c * 32;
+      for (int i = 0; i < np; ++i) {
+        const int col = col0 + 32 * i, tc = tc0 + 32 * i;
         if (col >= I) break;
         uint32_t g[32], u[32], w[16];
-        tmem_ld_32x32b_x32(tacc + c * 32, g);
-        tmem_ld_32x32b_x32(tacc + 128 + c * 32, u);
+        tmem_ld_32x32b_x32(tacc + tc, g);
+        tmem_ld_32x32b_x32(tacc + tc + uoff, u);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -413,13 +454,12 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
         }
       }
     } else if constexpr (kind_of(KIND) == kFwdDown || kind_of(KIND) == kDgradGateUp) {
-      constexpr int HP = Traits<KIND>::pieces / 2;
 #pragma unroll 1
-      for (int c = HP * half; c < HP * half + HP; ++c) {
-        const int col = x.n0 + c * 32;
+      for (int i = 0; i < np; ++i) {
+        const int col = col0 + 32 * i, tc = tc0 + 32 * i;
         if (col >= p.Nout) break;
         uint32_t v[32], w[16];
-        tmem_ld_32x32b_x32(tacc + c * 32, v);
+        tmem_ld_32x32b_x32(tacc + tc, v);
         tmem_ld_wait();
         pack32(v, w);
         const uint32_t b = ring.next(lane);
@@ -447,16 +487,15 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
           for (int q = 0; q < 4; ++q) a[q] = b[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       };
-      constexpr int HP = Traits<KIND>::pieces / 2;
-      fetch(x.n0 + half * HP * 32, rg, ru);
+      fetch(col0, rg, ru);
 #pragma unroll 1
-      for (int c = HP * half; c < HP * half + HP; ++c) {
-        const int col = x.n0 + c * 32;
+      for (int i = 0; i < np; ++i) {
+        const int col = col0 + 32 * i, tc = tc0 + 32 * i;
         if (col >= I) break;
         uint4 ng[4], nu[4];
-        fetch(c + 1 < HP * half + HP ? col + 32 : I, ng, nu);
+        fetch(i + 1 < np ? col + 32 : I, ng, nu);
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tacc + c * 32, v);
+        tmem_ld_32x32b_x32(tacc + tc, v);
         tmem_ld_wait();
         float g[32], u[32];
 #pragma unroll
@@ -666,7 +705,8 @@ __device__ __forceinline__ void produce_gathered(const Params& p, const int32_t*
 
 template <int KIND>
 __global__ void __launch_bounds__(Traits<KIND>::threads, 1)
-gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA64,
+              const __grid_constant__ CUtensorMap mapB0,
               const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapC0,
               const __grid_constant__ CUtensorMap mapC1, const Params p) {
   constexpr int STAGES = Traits<KIND>::stages;
@@ -732,6 +772,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapA);
+    if constexpr (PAIR) tma_prefetch_desc(&mapA64);
     tma_prefetch_desc(&mapB0);
     tma_prefetch_desc(&mapB1);
     tma_prefetch_desc(&mapC0);
@@ -784,13 +825,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       bool run = true;
       for (int t = t_first; run && t < total; t += t_step) {
         const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
-        // In a pair whose expert has an odd number of 128-row tiles the
-        // peer's rows all lie past the expert's end: its tile is computed
-        // but never stored, so its A rows are not loaded.
-        bool peer_idle = false;
-        if constexpr (PAIR) peer_idle = x.m0 - rank * BM + BM >= x.hi;
-        const bool load_a = !(PAIR && rank == 1 && peer_idle);
-        const uint32_t tx = PAIR ? 2 * STAGE_BYTES - (peer_idle ? A_BYTES : 0u) : STAGE_BYTES;
+        // Each CTA loads its A rows (64 in a half tile) and its half of B;
+        // the leader's barrier counts both CTAs.
+        const bool load_a = true;
+        const uint32_t tx =
+            PAIR ? 2 * (B_BYTES + (x.rows < BM ? A_BYTES / 2 : A_BYTES)) : STAGE_BYTES;
         for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1;
@@ -805,7 +844,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           } else {
             mbar_arrive_expect_tx(full_bar(s), tx);
           }
-          load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, fb, &mapA, &mapB0, &mapB1,
+          load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, fb, &mapA, &mapA64, &mapB0, &mapB1,
                            rank, load_a);
           issued[s] = (int)ph;
           if constexpr (Traits<KIND>::wgrad)
@@ -870,7 +909,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
                                                    : desc_sw128(sa + kk * (UK * 2), 16, 1024);
             const uint64_t bd = Traits<KIND>::b_mn ? desc_sw128(sb + kk * (UK * 128), MN_BOX_BYTES, 1024)
                                                    : desc_sw128(sb + kk * (UK * 2), 16, 1024);
-            if constexpr (PAIR) umma_f16_pair(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR)
+              umma_f16_pair(tacc, ad, bd, x.rows < BM ? Traits<KIND>::idesc_half : Traits<KIND>::idesc,
+                            (kb > 0 || kk > 0) ? 1u : 0u);
             else umma_f16(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           // the stage is free in both CTAs once these MMAs have read it
@@ -1019,7 +1060,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, c
 }
 
 template <int KIND>
-int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+int launch(const CUtensorMap& a, const CUtensorMap& a64, const CUtensorMap& b0, const CUtensorMap& b1,
            const CUtensorMap& c0, const CUtensorMap& c1, const Params& p, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -1032,7 +1073,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   if constexpr (CS == 1) {
     // One persistent CTA per SM.  A plain launch: the same kernel launched
     // through the cluster-attribute path (cluster size 1) measured ~20 % slower.
-    gmm_tc_kernel<KIND><<<sm_count(), Traits<KIND>::threads, Traits<KIND>::smem_bytes, s>>>(a, b0, b1, c0, c1, p);
+    gmm_tc_kernel<KIND><<<sm_count(), Traits<KIND>::threads, Traits<KIND>::smem_bytes, s>>>(a, a64, b0, b1, c0, c1, p);
     count_launches(1);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
@@ -1061,7 +1102,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   }
   if (resident > 0 && resident < clusters) clusters = resident;
   cfg.gridDim = dim3(clusters * CS, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gmm_tc_kernel<KIND>, a, b0, b1, c0, c1, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, gmm_tc_kernel<KIND>, a, a64, b0, b1, c0, c1, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -1077,21 +1118,23 @@ int device_ok() {
   return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
-// Whether a forward GEMM runs as CTA pairs, from the rows per expert.  A
-// pair wastes half a tile on every expert with an odd number of 128-row
-// tiles, and skewed routing has many of them.  GB300, H=2048, bf16, us,
-// pair / single:
-//   routing     rows/expert   gate/up (I=768|512)   down
-//   uniform         256         202 / 210          108 / 108
-//   uniform         512         318 / 323          167 / 172
-//   uniform        1024         562 / 577          289 / 304
-//   uniform        2048        1028 / 1069         531 / 569
-//   Zipf(1.2)       256         301 / 289          179 / 159
-//   Zipf(1.2)      1024         742 / 780          455 / 442
-// Gate/up pairs from 512 rows per expert, down pairs from 2048, so that
-// skewed routing never pays for them.
-constexpr long long kPairMinRowsGateUp = 512;
+// Whether a GEMM runs as CTA pairs, from the rows per expert (the routing's
+// skew is not known on the host without a sync).  With half tiles a pair
+// covers the same rows as single CTAs; what remains is how well each kind
+// uses a pair.  GB300, H=2048, bf16, us, pair / single:
+//   routing    rows/    gate/up (I=768|512)   gate/up      down        gate/up
+//              expert   saving (g, u)         not saving               dgrad
+//   uniform      256      196 / 209           188 / 195    108 / 108   189 / 194
+//   uniform      512      310 / 322           301 / 301    170 / 171   305 / 314
+//   uniform     1024      556 / 573           537 / 536    297 / 302   536 / 564
+//   Zipf(1.2)    256      294 / 289           281 / 270    175 / 159   291 / 285
+//   Zipf(1.2)   1024      737 / 778           710 / 723    448 / 440   779 / 806
+// (down at 2048 rows per expert, uniform: 531 / 569; the down dgrad, whose
+// SwiGLU-backward epilogue dominates, measured slower paired everywhere.)
+constexpr long long kPairMinRowsGateUpSave = 256;
+constexpr long long kPairMinRowsGateUp = 1024;
 constexpr long long kPairMinRowsDown = 2048;
+constexpr long long kPairMinRowsDgradGateUp = 256;
 inline bool use_pairs(long long min_rows, int N, int E) { return (long long)N >= min_rows * E; }
 
 Params base_params(const int32_t* off, int N, int E, int32_t* status) {
@@ -1130,8 +1173,12 @@ static int gate_up_bf16(const void* A, int T, const int32_t* gather, int K, cons
   CUtensorMap ma, mg, mu;
   const uint64_t da[2] = {(uint64_t)H, (uint64_t)(gather ? T : N)};
   const uint32_t ba[2] = {64, gather ? 1u : 128u};  // (not read when gathering)
+  // gathered A rows are loaded by the single-CTA producer only
+  const bool paired =
+      gather == nullptr &&
+      use_pairs(save != nullptr ? kPairMinRowsGateUpSave : kPairMinRowsGateUp, N, E);
   const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)E};
-  const uint32_t bw[3] = {64, 128, 1};
+  const uint32_t bw[3] = {64, paired ? 64u : 128u, 1};  // a pair CTA: 64 gate + 64 up rows
   if (!make_map(&ma, A, 2, da, ba) || !make_map(&mg, Wg, 3, dw, bw) || !make_map(&mu, Wu, 3, dw, bw))
     return MOE_ERR_CUDA;
   Params p = base_params(off, N, E, status);
@@ -1149,10 +1196,13 @@ static int gate_up_bf16(const void* A, int T, const int32_t* gather, int K, cons
   CUtensorMap c_act, c_save;
   if (!store_map_2d(&c_act, act, I, N) || !store_map_2d(&c_save, save ? save : act, save ? 2 * I : I, N))
     return MOE_ERR_CUDA;
-  // gathered A rows are loaded by the single-CTA producer only
-  return (gather == nullptr && use_pairs(kPairMinRowsGateUp, N, E))
-             ? launch<kFwdGateUp | kPaired>(ma, mg, mu, c_act, c_save, p, s)
-             : launch<kFwdGateUp>(ma, mg, mu, c_act, c_save, p, s);
+  CUtensorMap ma64 = ma;  // 64-row A boxes for a pair's half tiles
+  if (paired) {
+    const uint32_t b64[2] = {64, 64};
+    if (!make_map(&ma64, A, 2, da, b64)) return MOE_ERR_CUDA;
+  }
+  return paired ? launch<kFwdGateUp | kPaired>(ma, ma64, mg, mu, c_act, c_save, p, s)
+                : launch<kFwdGateUp>(ma, ma, mg, mu, c_act, c_save, p, s);
 }
 
 int launch_gmm_bf16_gate_up(const void* A, const void* Wg, const void* Wu, const int32_t* off,
@@ -1187,8 +1237,13 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   p.out = static_cast<__nv_bfloat16*>(out);
   CUtensorMap c_out;
   if (!store_map_2d(&c_out, out, H, N)) return MOE_ERR_CUDA;
-  return paired ? launch<kFwdDown | kPaired>(ma, md, md, c_out, c_out, p, s)
-                : launch<kFwdDown>(ma, md, md, c_out, c_out, p, s);
+  CUtensorMap ma64 = ma;
+  if (paired) {
+    const uint32_t b64[2] = {64, 64};
+    if (!make_map(&ma64, A, 2, da, b64)) return MOE_ERR_CUDA;
+  }
+  return paired ? launch<kFwdDown | kPaired>(ma, ma64, md, md, c_out, c_out, p, s)
+                : launch<kFwdDown>(ma, ma, md, md, c_out, c_out, p, s);
 }
 
 int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* off, int N, int H,
@@ -1212,7 +1267,7 @@ int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* o
   p.aux = static_cast<const __nv_bfloat16*>(gate_up);
   CUtensorMap c_dgu;
   if (!store_map_2d(&c_dgu, dgu, 2 * I, N)) return MOE_ERR_CUDA;
-  return launch<kDgradDown>(m_dy, m_wd, m_wd, c_dgu, c_dgu, p, s);
+  return launch<kDgradDown>(m_dy, m_dy, m_wd, m_wd, c_dgu, c_dgu, p, s);
 }
 
 int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H, int I, int E,
@@ -1236,7 +1291,15 @@ int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H,
   q.out = static_cast<__nv_bfloat16*>(dX);
   CUtensorMap c_dx;
   if (!store_map_2d(&c_dx, dX, H, N)) return MOE_ERR_CUDA;
-  return launch<kDgradGateUp>(m_dgu, m_wg, m_wu, c_dx, c_dx, q, s);
+  const bool paired = use_pairs(kPairMinRowsDgradGateUp, N, E);
+  CUtensorMap m_dgu64 = m_dgu;  // 64-row A boxes for a pair's half tiles
+  if (paired) {
+    const uint32_t b64[2] = {64, 64};
+    if (!make_map(&m_dgu64, dgu, 2, d_dgu, b64)) return MOE_ERR_CUDA;
+  }
+  return paired
+             ? launch<kDgradGateUp | kPaired>(m_dgu, m_dgu64, m_wg, m_wu, c_dx, c_dx, q, s)
+             : launch<kDgradGateUp>(m_dgu, m_dgu, m_wg, m_wu, c_dx, c_dx, q, s);
 }
 
 // With no rows at all the operand maps are never read (every tile has zero
@@ -1261,7 +1324,7 @@ int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, 
   p.out = static_cast<__nv_bfloat16*>(dWd);
   CUtensorMap c_dwd;
   if (!store_map_3d(&c_dwd, dWd, I, H, E)) return MOE_ERR_CUDA;
-  return launch<kWgradDown>(m_a, m_b, m_b, c_dwd, c_dwd, p, s);
+  return launch<kWgradDown>(m_a, m_a, m_b, m_b, c_dwd, c_dwd, p, s);
 }
 
 // Gate/up wgrad.  gather == nullptr: X is the permuted [N, H] buffer;
@@ -1297,7 +1360,7 @@ static int gate_up_wgrad_bf16(const void* dgu, const void* X, int T, const int32
   CUtensorMap c_dwg, c_dwu;
   if (!store_map_3d(&c_dwg, dWg, H, I, E) || !store_map_3d(&c_dwu, dWu, H, I, E))
     return MOE_ERR_CUDA;
-  return launch<kWgradGateUp>(m_a, m_b, m_b, c_dwg, c_dwu, p, s);
+  return launch<kWgradGateUp>(m_a, m_a, m_b, m_b, c_dwg, c_dwu, p, s);
 }
 
 int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
