@@ -16,11 +16,15 @@
 //     accumulates into the other one, apply the epilogue, stage bf16 in
 //     shared memory and write it with TMA stores;
 //   * the wgrads add a warp that zeroes expert tail rows in shared memory;
-//   * the forward kinds also come as CTA pairs (tcgen05 cta_group::2, a
-//     2-CTA cluster on one TPC, M=256 per MMA, half of the B tile per CTA,
-//     6-stage ring), chosen per call from the rows per expert.
+//   * gate/up, down and the gate/up dgrad also come as CTA pairs (tcgen05
+//     cta_group::2, a 2-CTA cluster on one TPC, M=256 per MMA, half of the
+//     B tile per CTA, 6-stage ring; an expert's last <= 128 rows as an M=128
+//     half tile), chosen per call and kind from the rows per expert;
+//   * the forward gate/up and its wgrad can also read the token matrix
+//     through sorted_indices themselves (the producer warp gathers rows with
+//     cp.async) instead of the permuted copy.
 //
-// Six variants (KIND) share the machinery:
+// Six kinds (KIND; + kPaired for the CTA-pair form) share the machinery:
 //   FwdGateUp   act = silu(X Wg^T) * (X Wu^T)       B tile = 128 rows of Wg
 //                                                   + 128 rows of Wu
 //   FwdDown     expanded = act Wd^T
@@ -101,11 +105,12 @@ struct Traits {
   static constexpr uint32_t idesc = idesc_bf16_f32(BM * cs, bn, a_mn, b_mn);
   // a pair's half tile: M=128 over the pair, 64 A rows per CTA
   static constexpr uint32_t idesc_half = idesc_bf16_f32(BM, bn, a_mn, b_mn);
-  // k-block depth and ring depth: 64-deep blocks (one 128-byte swizzle row)
-  // in 4 stages for every kind.  Measured on GB300: a fourth stage beats a
-  // second staging unit per epilogue warp, and for the wgrads 32-deep blocks
-  // in 8 stages (a ring holding two tiles) lose more to the smaller TMA
-  // boxes than they gain from overlap.
+  // k-block depth and ring depth: 64-deep blocks (one 128-byte swizzle row);
+  // single CTAs hold 4 stages of 48 KB (3 for the down dgrad, below), pairs
+  // 6 of 32 KB.  Measured on GB300: a fourth stage beats a second staging
+  // unit per epilogue warp, and for the wgrads 32-deep blocks in 8 stages (a
+  // ring holding two tiles) lose more to the smaller TMA boxes than they
+  // gain from overlap.
   static constexpr int bk = 64;
   // The SwiGLU-backward epilogue stages two units (dg, du) per piece and is
   // the slower side of its kernel: it trades a stage for a two-unit ring.
@@ -230,14 +235,14 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
 }
 
 // TMA loads of k block kb of tile x into one stage: this CTA's own 128 rows
-// of A (unless load_a is false) and its part of B: all of it for a single
+// of A (64 in a pair's half tile) and its part of B: all of it for a single
 // CTA, the rank-th half (128 of the 256 N rows) in a pair.  `bar` receives
 // the bytes: this CTA's full barrier, or the leader's in a pair.
 template <int KIND>
 __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& p, uint32_t sa,
                                            uint32_t sb, uint32_t bar, const CUtensorMap* mA,
                                            const CUtensorMap* mA64, const CUtensorMap* mB0,
-                                           const CUtensorMap* mB1, int rank, bool load_a) {
+                                           const CUtensorMap* mB1, int rank) {
   constexpr bool PAIR = Traits<KIND>::pair;
   constexpr int B_ROWS = Traits<KIND>::b_rows;
   constexpr uint32_t MN_BOX_BYTES = Traits<KIND>::mn_box;
@@ -257,7 +262,7 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
     // B tile = 128 rows of W_gate, then the same 128 rows of W_up; in a pair
     // each CTA holds 64 gate rows then the same 64 up rows (its N half), so
     // that gate and up of one output column meet in one thread
-    if (load_a) l2(sa, mAr, k0, x.m0);
+    l2(sa, mAr, k0, x.m0);
     if constexpr (PAIR) {
       l3(sb, mB0, k0, x.n0 + 64 * rank, x.e);
       l3(sb + Traits<KIND>::b_bytes / 2, mB1, k0, x.n0 + 64 * rank, x.e);
@@ -266,14 +271,14 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
       l3(sb + Traits<KIND>::b_bytes / 2, mB1, k0, x.n0, x.e);
     }
   } else if constexpr (kind_of(KIND) == kFwdDown) {
-    if (load_a) l2(sa, mAr, k0, x.m0);
+    l2(sa, mAr, k0, x.m0);
     l3(sb, mB0, k0, nb, x.e);  // B_ROWS rows of the W_down panel in one box
   } else if constexpr (kind_of(KIND) == kDgradDown) {
-    if (load_a) l2(sa, mAr, k0, x.m0);
+    l2(sa, mAr, k0, x.m0);
 #pragma unroll
     for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, k0, x.e);
   } else if constexpr (kind_of(KIND) == kDgradGateUp) {
-    if (load_a) l2(sa, mAr, k0, x.m0);
+    l2(sa, mAr, k0, x.m0);
     const bool up = k0 >= p.I;
     const int kk = up ? k0 - p.I : k0;
 #pragma unroll
@@ -382,7 +387,8 @@ __device__ __forceinline__ void flush_unit(uint32_t buf, int lane, bool tma, con
 }
 
 // Epilogue of one tile for one epilogue warp.  tacc: TMEM address of the
-// warp's lane quarter of the accumulator; quarter: which 32 rows.
+// warp's lane quarter of the accumulator; quarter: that lane quarter; half:
+// which of the quarter's two warps.
 template <int KIND>
 __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_t tacc, int quarter,
                                          int half, int lane, Ring<Traits<KIND>::nbuf>& ring,
@@ -827,7 +833,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
         // Each CTA loads its A rows (64 in a half tile) and its half of B;
         // the leader's barrier counts both CTAs.
-        const bool load_a = true;
         const uint32_t tx =
             PAIR ? 2 * (B_BYTES + (x.rows < BM ? A_BYTES / 2 : A_BYTES)) : STAGE_BYTES;
         for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
@@ -845,7 +850,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             mbar_arrive_expect_tx(full_bar(s), tx);
           }
           load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, fb, &mapA, &mapA64, &mapB0, &mapB1,
-                           rank, load_a);
+                           rank);
           issued[s] = (int)ph;
           if constexpr (Traits<KIND>::wgrad)
             if (k_tail<KIND>(x, kb).zl > 0) mbar_arrive(tail_bar(s));
