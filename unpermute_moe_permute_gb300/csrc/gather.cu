@@ -218,12 +218,17 @@ combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
   const int nvec = H / EL;
   for (int v = lane; v < nvec; v += 32) {
     const size_t col = (size_t)v * EL;
+    // every load of this column chunk is issued before any arithmetic, so an
+    // iteration waits for one memory round trip
     uint4 x[KMAX];
 #pragma unroll
     for (int k = 0; k < KMAX; ++k)
       if (kind[k] == kRouted) x[k] = ld_nc_v4(Y + (size_t)arg[k] * H + col);
+    uint4 ov = make_uint4(0u, 0u, 0u, 0u), sv = make_uint4(0u, 0u, 0u, 0u);
+    if (need_ori) ov = ld_nc_v4(ori_x + (size_t)t * H + col);
+    if (shared_x != nullptr) sv = ld_nc_v4(shared_x + (size_t)t * H + col);
     float ori[EL];
-    if (need_ori) VT::unpack(ld_nc_v4(ori_x + (size_t)t * H + col), ori);
+    if (need_ori) VT::unpack(ov, ori);
     float acc[EL];
 #pragma unroll
     for (int e = 0; e < EL; ++e) acc[e] = 0.f;
@@ -250,7 +255,7 @@ combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
     }
     if (shared_x != nullptr) {
       float sh[EL];
-      VT::unpack(ld_nc_v4(shared_x + (size_t)t * H + col), sh);
+      VT::unpack(sv, sh);
 #pragma unroll
       for (int e = 0; e < EL; ++e) acc[e] += sh[e];
     }
