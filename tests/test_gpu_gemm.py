@@ -185,6 +185,43 @@ def test_bf16_layer_backward(lib, kw):
         assert not np64(g["dWd"][int(e)]).any() and not np64(g["dWg"][int(e)]).any()
 
 
+def _down_dgrad_last_wave_split(tiles: int, grid: int) -> int:
+    """How the down dgrad splits its last wave along N: when the tiles leave a
+    last wave that fills at most half of the persistent grid (one CTA per
+    SM), each of its tiles becomes 4 (at most a quarter full) or 2 narrower
+    tiles; 1 = no split."""
+    left = tiles % grid
+    if left == 0 or 2 * left > grid:
+        return 1
+    return 4 if 4 * left <= grid else 2
+
+
+@pytest.mark.parametrize("T,split", [(850, 4), (1000, 2), (1200, 1)])
+def test_bf16_layer_backward_down_dgrad_last_wave(lib, T, split):
+    """K = E = 8 gives every expert exactly T rows, so the down dgrad has
+    8 * ceil(T/128) * 3 tiles (I = 768): with 152 SMs, 168 tiles (a last wave
+    of 16, split 4 ways), 192 (40, split 2 ways) and 240 (88, not split).  The
+    backward is checked on every row of d_permuted and every expert's weight
+    grads, which all depend on the down dgrad's output."""
+    E, K, I, H = 8, 8, 768, 256
+    tiles = E * -(-T // 128) * (I // 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if _down_dgrad_last_wave_split(tiles, sms) != split:
+        pytest.skip(f"{sms} SMs: this shape does not give the intended last wave")
+    d = moe_inputs.layer_fwd_bwd(3, T=T, H=H, E=E, K=K, I=I)
+    g = _gpu_layer_fwd_bwd(lib, d)
+    (si, rm, tpe, off), perm, act, expd, _, _ = _oracle_forward(d)
+    assert (tpe == T).all()
+    gexp, _ = O.unpermute_grad(np64(d["grad_out"]), expd, rm, d["probs"].numpy(), T, K, "bf16")
+    dperm, dWg, dWu, dWd = O.expert_mlp_grad(gexp, perm, act, off, np64(d["W_gate"]),
+                                             np64(d["W_up"]), np64(d["W_down"]), "bf16")
+    assert_normwise(np64(g["dperm"]), dperm, BF16_TOL, "d_permuted")
+    for e in range(E):
+        assert_normwise(np64(g["dWg"][e]), dWg[e], BF16_TOL, f"dW_gate[{e}]")
+        assert_normwise(np64(g["dWu"][e]), dWu[e], BF16_TOL, f"dW_up[{e}]")
+        assert_normwise(np64(g["dWd"][e]), dWd[e], BF16_TOL, f"dW_down[{e}]")
+
+
 def test_bf16_mlp_grad_without_rows_writes_zero_weight_grads(lib):
     E, H, I = 3, 128, 64
     Wg = torch.randn(E, I, H, device=DEV).bfloat16()

@@ -171,7 +171,31 @@ struct Tile {
   int m0, n0;     // first output row / column of the tile
   int kblocks;    // 64-deep k blocks
   int rows;       // A rows this CTA owns: 128, or 64 in a pair's half tile
+  int nw;         // UMMA N of the tile: 256, or 128 / 64 for a split last-wave tile
 };
+
+// Last-wave split (down dgrad): when the tiles leave a last wave that fills
+// at most half of the persistent grid, each of its tiles is split along N
+// into `split` narrower tiles (N = 128 or 64), so that 2x or 4x as many SMs
+// share it.  Tile slots [0, tail0) are whole tiles; slot tail0 + u is part
+// u % split of whole tile tail0 + u / split.
+struct Waves {
+  int tail0, split, slots;
+};
+
+template <int KIND>
+__device__ __forceinline__ Waves plan_waves(int total, int grid) {
+  Waves w{total, 1, total};
+  if constexpr (kind_of(KIND) == kDgradDown) {
+    const int left = total % grid;
+    if (left > 0 && 2 * left <= grid) {
+      w.split = 4 * left <= grid ? 4 : 2;
+      w.tail0 = total - left;
+      w.slots = w.tail0 + left * w.split;
+    }
+  }
+  return w;
+}
 
 // Wgrad k block kb of tile x (k = the expert's token rows): the MMAs cover
 // nk 16-row groups; rows [z0, z0 + zl) of the block lie inside the last of
@@ -217,6 +241,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.m0 = g0 + rank * x.rows;
     x.n0 = nt * Traits<KIND>::n_per_tile;
     x.kblocks = p.Kd / Traits<KIND>::bk;
+    x.nw = Traits<KIND>::bn;
   } else {
     const int m_groups = (p.m_tiles + CS - 1) / CS;
     const int per = m_groups * p.n_tiles;
@@ -230,7 +255,20 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int32_
     x.rows = BM;
     x.n0 = nt * Traits<KIND>::bn;
     x.kblocks = (r.hi - r.lo + Traits<KIND>::bk - 1) / Traits<KIND>::bk;
+    x.nw = Traits<KIND>::bn;
   }
+  return x;
+}
+
+// Tile slot t of the plan w (see Waves).
+template <int KIND>
+__device__ __forceinline__ Tile decode_slot(int t, const Waves& w, const Params& p,
+                                            const int32_t* prefix, const int32_t* offs, int rank) {
+  if (t < w.tail0) return decode_tile<KIND>(t, p, prefix, offs, rank);
+  const int u = t - w.tail0;
+  Tile x = decode_tile<KIND>(w.tail0 + u / w.split, p, prefix, offs, rank);
+  x.nw = Traits<KIND>::bn / w.split;
+  x.n0 += (u % w.split) * x.nw;
   return x;
 }
 
@@ -276,7 +314,8 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
   } else if constexpr (kind_of(KIND) == kDgradDown) {
     l2(sa, mAr, k0, x.m0);
 #pragma unroll
-    for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, k0, x.e);
+    for (int j = 0; j < B_ROWS / 64; ++j)
+      if (j * 64 < x.nw) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, k0, x.e);
   } else if constexpr (kind_of(KIND) == kDgradGateUp) {
     l2(sa, mAr, k0, x.m0);
     const bool up = k0 >= p.I;
@@ -418,7 +457,7 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
         np = 1, tc0 = 32 * half, uoff = 64, col0 = x.n0 + 64 * blk + 32 * half;
       }
     } else {
-      if (!halft) np = 4, tc0 = 128 * half, col0 = x.n0 + 128 * half;
+      if (!halft) np = x.nw / 64, tc0 = (x.nw / 2) * half, col0 = x.n0 + (x.nw / 2) * half;
       else np = 2, tc0 = 64 * half, col0 = x.n0 + 128 * blk + 64 * half;
     }
     if (r0 >= x.hi) return;  // warp-uniform: no row of this warp is valid
@@ -815,6 +854,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
   const int t_first = CS > 1 ? (int)cluster_id_x() : (int)blockIdx.x;
   const int t_step = CS > 1 ? (int)cluster_count_x() : (int)gridDim.x;
+  const Waves wv = plan_waves<KIND>(total, t_step);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -829,12 +869,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       for (int s = 0; s < STAGES; ++s) issued[s] = -1;
       int g = 0;
       bool run = true;
-      for (int t = t_first; run && t < total; t += t_step) {
-        const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
+      for (int t = t_first; run && t < wv.slots; t += t_step) {
+        const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
         // Each CTA loads its A rows (64 in a half tile) and its half of B;
-        // the leader's barrier counts both CTAs.
+        // the leader's barrier counts both CTAs.  A split tile loads only
+        // the B boxes of its columns.
         const uint32_t tx =
-            PAIR ? 2 * (B_BYTES + (x.rows < BM ? A_BYTES / 2 : A_BYTES)) : STAGE_BYTES;
+            PAIR ? 2 * (B_BYTES + (x.rows < BM ? A_BYTES / 2 : A_BYTES))
+                 : A_BYTES + B_BYTES / Traits<KIND>::bn * (uint32_t)x.nw;
         for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1;
@@ -872,8 +914,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     int g = 0, it = 0;
     uint32_t fixph = 0;  // bit s: parity of the next fix_bar(s) phase
     bool run = true;
-    for (int t = t_first; run && t < total; t += t_step, ++it) {
-      const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
+    for (int t = t_first; run && t < wv.slots; t += t_step, ++it) {
+      const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
+      const uint32_t idesc = x.nw == Traits<KIND>::bn ? Traits<KIND>::idesc
+                                                     : idesc_bf16_f32(BM, x.nw, Traits<KIND>::a_mn,
+                                                                      Traits<KIND>::b_mn);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
@@ -917,7 +962,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             if constexpr (PAIR)
               umma_f16_pair(tacc, ad, bd, x.rows < BM ? Traits<KIND>::idesc_half : Traits<KIND>::idesc,
                             (kb > 0 || kk > 0) ? 1u : 0u);
-            else umma_f16(tacc, ad, bd, Traits<KIND>::idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            else umma_f16(tacc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           // the stage is free in both CTAs once these MMAs have read it
           if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
@@ -945,8 +990,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
     Ring<NBUF> ring{staging + (uint32_t)(warp - 2) * NBUF * UNIT_BYTES, 0};
     int it = 0;
-    for (int t = t_first; t < total; t += t_step, ++it) {
-      const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
+    for (int t = t_first; t < wv.slots; t += t_step, ++it) {
+      const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))) break;
@@ -973,8 +1018,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     int g = 0;
     uint32_t tph = 0;  // bit s: parity of the next tail_bar(s) phase
     bool run = true;
-    for (int t = t_first; run && t < total; t += t_step) {
-      const Tile x = decode_tile<KIND>(t, p, prefix, offs, rank);
+    for (int t = t_first; run && t < wv.slots; t += t_step) {
+      const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
       for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
         const KTail kt = k_tail<KIND>(x, kb);
         if (kt.zl == 0) continue;
