@@ -186,10 +186,10 @@ def test_bf16_layer_backward(lib, kw):
 
 
 def _down_dgrad_last_wave_split(tiles: int, grid: int) -> int:
-    """How the down dgrad splits its last wave along N: when the tiles leave a
-    last wave that fills at most half of the persistent grid (one CTA per
-    SM), each of its tiles becomes 4 (at most a quarter full) or 2 narrower
-    tiles; 1 = no split."""
+    """How the single-CTA down projection and dgrads split their last wave
+    along N: when the tiles leave a last wave that fills at most half of the
+    persistent grid (one CTA per SM), each of its tiles becomes 4 (at most a
+    quarter full) or 2 narrower tiles; 1 = no split."""
     left = tiles % grid
     if left == 0 or 2 * left > grid:
         return 1
@@ -219,6 +219,32 @@ def test_bf16_layer_backward_down_dgrad_last_wave(lib, T, split):
     for e in range(E):
         assert_normwise(np64(g["dWg"][e]), dWg[e], BF16_TOL, f"dW_gate[{e}]")
         assert_normwise(np64(g["dWu"][e]), dWu[e], BF16_TOL, f"dW_up[{e}]")
+        assert_normwise(np64(g["dWd"][e]), dWd[e], BF16_TOL, f"dW_down[{e}]")
+
+
+def test_bf16_layer_split_last_waves_with_full_waves(lib):
+    """T=800 H=2048 E=32 K=8 I=256: fewer than 256 rows per expert, so the
+    down projection and the gate/up dgrad run single-CTA, each with 512
+    tiles (64 m-tiles x 8 n-tiles): with 152 SMs, three full waves and a last
+    wave of 56 tiles split 2 ways.  Forward and backward on every row and
+    every expert against the oracle."""
+    d = moe_inputs.layer_fwd_bwd(5, T=800, H=2048, E=32, K=8, I=256)
+    T, K, E = d["T"], d["K"], d["E"]
+    (si, rm, tpe, off), perm, act, expd, _, _ = _oracle_forward(d)
+    tiles = int(np.sum(-(-tpe // 128))) * (2048 // 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if tiles < sms or _down_dgrad_last_wave_split(tiles, sms) == 1:
+        pytest.skip(f"{sms} SMs: this shape does not give a split last wave after full waves")
+    assert tpe.max() < 256                               # single-CTA gate/up dgrad
+    g = _gpu_layer_fwd_bwd(lib, d)
+    N = len(si)
+    assert_normwise(np64(g["expanded"])[:N], O.round_to_bf16(expd), BF16_TOL, "expanded")
+    gexp, _ = O.unpermute_grad(np64(d["grad_out"]), expd, rm, d["probs"].numpy(), T, K, "bf16")
+    dperm, dWg, dWu, dWd = O.expert_mlp_grad(gexp, perm, act, off, np64(d["W_gate"]),
+                                             np64(d["W_up"]), np64(d["W_down"]), "bf16")
+    assert_normwise(np64(g["dperm"])[:N], dperm, BF16_TOL, "d_permuted")
+    for e in range(E):
+        assert_normwise(np64(g["dWg"][e]), dWg[e], BF16_TOL, f"dW_gate[{e}]")
         assert_normwise(np64(g["dWd"][e]), dWd[e], BF16_TOL, f"dW_down[{e}]")
 
 

@@ -174,11 +174,12 @@ struct Tile {
   int nw;         // UMMA N of the tile: 256, or 128 / 64 for a split last-wave tile
 };
 
-// Last-wave split (down dgrad): when the tiles leave a last wave that fills
-// at most half of the persistent grid, each of its tiles is split along N
-// into `split` narrower tiles (N = 128 or 64), so that 2x or 4x as many SMs
-// share it.  Tile slots [0, tail0) are whole tiles; slot tail0 + u is part
-// u % split of whole tile tail0 + u / split.
+// Last-wave split (single-CTA down projection and dgrads): when the
+// tiles leave a last wave that fills at most half of the persistent grid,
+// each of its tiles is split along N into `split` narrower tiles (N = 128 or
+// 64), so that 2x or 4x as many SMs share it.  Tile slots [0, tail0) are
+// whole tiles; slot tail0 + u is part u % split of whole tile
+// tail0 + u / split.
 struct Waves {
   int tail0, split, slots;
 };
@@ -186,7 +187,7 @@ struct Waves {
 template <int KIND>
 __device__ __forceinline__ Waves plan_waves(int total, int grid) {
   Waves w{total, 1, total};
-  if constexpr (kind_of(KIND) == kDgradDown) {
+  if constexpr (kind_of(KIND) == kDgradDown || KIND == kFwdDown || KIND == kDgradGateUp) {
     const int left = total % grid;
     if (left > 0 && 2 * left <= grid) {
       w.split = 4 * left <= grid ? 4 : 2;
@@ -310,7 +311,15 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
     }
   } else if constexpr (kind_of(KIND) == kFwdDown) {
     l2(sa, mAr, k0, x.m0);
-    l3(sb, mB0, k0, nb, x.e);  // B_ROWS rows of the W_down panel in one box
+    if (PAIR || x.nw == Traits<KIND>::bn) {
+      l3(sb, mB0, k0, nb, x.e);  // B_ROWS rows of the W_down panel in one box
+    } else {
+      // a split tile: its rows in 64-row boxes (mB1), which stack into the
+      // same swizzled layout as the whole box
+#pragma unroll
+      for (int j = 0; j < B_ROWS / 64; ++j)
+        if (j * 64 < x.nw) l3(sb + j * 8192u, mB1, k0, nb + j * 64, x.e);
+    }
   } else if constexpr (kind_of(KIND) == kDgradDown) {
     l2(sa, mAr, k0, x.m0);
 #pragma unroll
@@ -321,7 +330,8 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
     const bool up = k0 >= p.I;
     const int kk = up ? k0 - p.I : k0;
 #pragma unroll
-    for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, nb + j * 64, kk, x.e);
+    for (int j = 0; j < B_ROWS / 64; ++j)
+      if (j * 64 < x.nw) l3(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, nb + j * 64, kk, x.e);
   } else {  // wgrad: both operands MN-major, k = token rows of the expert
     const int row = x.lo + k0;
 #pragma unroll
@@ -1291,9 +1301,13 @@ int launch_gmm_bf16_down(const void* A, const void* Wd, const int32_t* off, int 
   if (paired) {
     const uint32_t b64[2] = {64, 64};
     if (!make_map(&ma64, A, 2, da, b64)) return MOE_ERR_CUDA;
+    return launch<kFwdDown | kPaired>(ma, ma64, md, md, c_out, c_out, p, s);
   }
-  return paired ? launch<kFwdDown | kPaired>(ma, ma64, md, md, c_out, c_out, p, s)
-                : launch<kFwdDown>(ma, ma, md, md, c_out, c_out, p, s);
+  // 64-row boxes of W_down for the split tiles of a short last wave
+  CUtensorMap md64;
+  const uint32_t bw64[3] = {64, 64, 1};
+  if (!make_map(&md64, Wd, 3, dw, bw64)) return MOE_ERR_CUDA;
+  return launch<kFwdDown>(ma, ma, md, md64, c_out, c_out, p, s);
 }
 
 int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* off, int N, int H,
