@@ -162,7 +162,8 @@ def _gpu_layer_fwd_bwd(lib, d):
                 dWg=dWg, dWu=dWu, dWd=dWd, gtok=gtok)
 
 
-@pytest.mark.parametrize("kw", SMALL + [dict(T=300, H=192, E=6, K=3, I=320)])
+@pytest.mark.parametrize("kw", SMALL + [dict(T=300, H=192, E=6, K=3, I=320),
+                                  dict(T=200, H=128, E=256, K=4, I=128)])  # many small experts
 def test_bf16_layer_backward(lib, kw):
     d = moe_inputs.layer_fwd_bwd(2, **kw)
     T, K, E = d["T"], d["K"], d["E"]
