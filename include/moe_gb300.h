@@ -125,10 +125,17 @@ int moe_check_status(const int32_t* dev_status, cudaStream_t stream);
  *                   bytes: ceil(T*K/512) blocks of E int32 expert counts
  *                   (padded to 8 bytes), then one 8-byte completion flag
  *                   per block.  Its contents need no clearing: each call
- *                   stamps the flags with a value no earlier call used.
+ *                   stamps the flags with a value no earlier call of the
+ *                   process used (seeded from the clock, the process id and
+ *                   a random draw, so a stamp left by another process
+ *                   matches only by a 64-bit coincidence).
  *   dev_status      optional; receives MOE_ERR_BAD_ID for an id outside
  *                   [0, E + num_special) or repeated within a row (the slot
- *                   is then treated as not dispatched)
+ *                   is then treated as not dispatched), and MOE_ERR_TIMEOUT
+ *                   if the one-launch routing's bounded wait for its other
+ *                   blocks ran out (then the waiting blocks' slots get
+ *                   row_map -1 and are not copied; the result is incomplete
+ *                   but no write leaves the output buffers)
  */
 size_t moe_permute_workspace_size(int T, int K, int E);
 int moe_permute(const void* tokens, int dtype, const int32_t* expert_ids, int T, int H, int K,
@@ -178,6 +185,18 @@ int moe_permute_masked(const void* tokens, int dtype, const int32_t* expert_ids,
                        void* permuted, int32_t* sorted_indices, int32_t* row_map,
                        int32_t* tokens_per_expert, int32_t* expert_offsets, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
+/* The row copy of moe_permute on its own, for a routing the caller already
+ * holds (a second tensor permuted the same way, or a routing rebuilt with
+ * moe_invert_sorted_indices):
+ *   permuted[row_map[t*K+k]] = tokens[t]          (exact copy)
+ * tokens [T, H] dtype, row_map [T*K] int32, permuted [N, H] dtype (N = rows
+ * of the buffer).  Slots whose row_map entry lies outside [0, N) (-1 marks a
+ * slot that is not dispatched) are skipped, so no entry can address memory
+ * outside permuted; rows no slot maps to are not written.  Row gather of
+ * hyper_parallel expert_parallel.py, _permute (x[permuted_indices]). */
+int moe_permute_rows(const void* tokens, int dtype, const int32_t* row_map, int T, int H, int K,
+                     int N, void* permuted, cudaStream_t stream);
 
 /* Rebuild row_map [TK] from sorted_indices [N] (row_map[sorted[i]] = i,
  * every other entry -1).  For callers that keep only sorted_indices. */
@@ -295,7 +314,8 @@ int moe_permute_grad(const void* grad_permuted, int dtype, const int32_t* row_ma
  *          = alpha1[j] * ori_x[t] + alpha2[j] * const_v[j],  j = id-E-Z-C    (const)
  * shared_x [T,H] nullable; ori_x [T,H] required when copy_num + const_num > 0;
  * alpha1/alpha2/const_v [const_num, H] (dtype) required when const_num > 0.
- * Ids outside [0, E+Z+C+Cn) set MOE_ERR_BAD_ID and contribute 0.
+ * Ids outside [0, E+Z+C+Cn) set MOE_ERR_BAD_ID and contribute 0; so does a
+ * routed slot (id < E) whose row_map entry lies outside [0, N).
  */
 int moe_combine(const void* expanded, int dtype, const int32_t* row_map, const int32_t* expert_ids,
                 const float* scales, const void* shared_x, const void* ori_x, int T, int H, int K,
@@ -304,8 +324,10 @@ int moe_combine(const void* expanded, int dtype, const int32_t* row_map, const i
                 cudaStream_t stream);
 
 /* moe_combine with the activity mask of moe_permute_masked: a slot (or every
- * slot of a token) masked off contributes nothing to the weighted sum; the
- * shared-expert term is still added.  active_mask NULL = moe_combine. */
+ * slot of a token) masked off contributes nothing to the weighted sum, and
+ * its row_map entry is not read (moe_permute_masked gives it -1); its id must
+ * still lie in [0, E+Z+C+Cn), else MOE_ERR_BAD_ID.  The shared-expert term is
+ * still added.  active_mask NULL = moe_combine. */
 int moe_combine_masked(const void* expanded, int dtype, const int32_t* row_map,
                        const int32_t* expert_ids, const float* scales, const void* shared_x,
                        const void* ori_x, const uint8_t* active_mask, int mask_dims, int T, int H,
@@ -324,7 +346,10 @@ int moe_combine_masked(const void* expanded, int dtype, const int32_t* row_map,
  *   *total      = sum of counts (device int32)
  * If total > capacity nothing is written to indices and dev_status gets
  * MOE_ERR_CAPACITY.  R*E <= 2048 (the combine_v2 constraint on local experts
- * times EP size); the sum of counts must stay below 2^31.
+ * times EP size).  The counts are summed in 64 bits first: if the sum of all
+ * counts does not fit in int32, nothing but *total = -1 is written and
+ * dev_status gets MOE_ERR_CAPACITY.  Negative counts count as 0 and set
+ * MOE_ERR_INVALID_ARG.
  */
 int moe_permute_indices(const int32_t* counts, int R, int E, int32_t* indices, int capacity,
                         int32_t* tokens_per_expert, int32_t* total, int32_t* dev_status,

@@ -60,6 +60,7 @@ _SIGNATURES = {
     "moe_combine_masked": ([_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                             _P, _P, _P, _P, _P, _P], _I),
     "moe_invert_sorted_indices": ([_P, _I, _I, _P, _P], _I),
+    "moe_permute_rows": ([_P, _I, _P, _I, _I, _I, _I, _P, _P], _I),
     "moe_permute_static_scratch": ([_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P],
                                    _I),
     "moe_gate_up_swiglu": ([_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
@@ -150,6 +151,11 @@ def _check(t: Optional[torch.Tensor], dtype, name: str):
 def new_status(device=None) -> torch.Tensor:
     """A zeroed device status word for the dev_status arguments."""
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def status_name(status: int) -> str:
+    """Name of a status code (moe_status_string)."""
+    return load_library().moe_status_string(int(status)).decode()
 
 
 def moe_selftest_bounded_wait(dev_status) -> None:
@@ -263,6 +269,18 @@ def moe_permute_static_scratch(tokens: Optional[torch.Tensor], expert_ids: torch
           num_experts, num_special, _ptr(permuted), _ptr(sorted_indices), _ptr(row_map),
           _ptr(tokens_per_expert), _ptr(expert_offsets), _ptr(dev_status), _stream())
     return PermuteResult(permuted, sorted_indices, row_map, tokens_per_expert, expert_offsets)
+
+
+def moe_permute_rows(tokens, row_map, K: int, N: int, *, permuted=None):
+    """permuted[row_map[t*K+k]] = tokens[t] for a routing the caller holds;
+    slots whose row lies outside [0, N) are skipped."""
+    _check(row_map, torch.int32, "row_map")
+    T, H = tokens.shape
+    if permuted is None:
+        permuted = torch.empty((N, H), dtype=tokens.dtype, device=tokens.device)
+    _call("moe_permute_rows", _ptr(tokens), _dtype(tokens), _ptr(row_map), T, H, K, N,
+          _ptr(permuted), _stream())
+    return permuted
 
 
 def moe_invert_sorted_indices(sorted_indices: torch.Tensor, N: int, TK: int, *, row_map=None):

@@ -183,26 +183,30 @@ combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
     const int id = ids[(size_t)t * K + lane];
     my_s = scales[(size_t)t * K + lane];
     const long long zlo = E, clo = zlo + zero_num, klo = clo + copy_num, khi = klo + const_num;
-    if (id >= 0 && id < E) {
+    // A slot masked off takes no part: it adds nothing, like a zero expert,
+    // and the permute gave it no row (row_map -1).  Its id must still lie in
+    // [0, E + Z + C + Cn).
+    const bool active =
+        active_mask == nullptr ||
+        (mask_dims == 1 ? active_mask[t] : active_mask[(size_t)t * K + lane]) != 0;
+    if (id < 0 || (long long)id >= khi) {
+      my_kind = kBad;
+    } else if (!active || (id >= zlo && id < clo)) {
+      my_kind = kZero;
+    } else if (id < E) {
+      // a routed slot must have a row inside the expert-major buffer
       const int r = row_map[(size_t)t * K + lane];
       if (r >= 0 && r < N) {
         my_kind = kRouted;
         my_arg = r;
       }
-    } else if (id >= zlo && id < clo) {
-      my_kind = kZero;
-    } else if (id >= clo && id < klo) {
+    } else if (id < klo) {
       my_kind = kCopy;
-    } else if (id >= klo && id < khi) {
+    } else {
       my_kind = kConst;
       my_arg = (int)(id - klo);
     }
     if (my_kind == kBad) set_status(status, MOE_ERR_BAD_ID);
-    // a slot masked off takes no part: it adds nothing, like a zero expert
-    if (active_mask != nullptr && my_kind != kBad) {
-      const uint8_t a = mask_dims == 1 ? active_mask[t] : active_mask[(size_t)t * K + lane];
-      if (a == 0) my_kind = kZero;
-    }
   }
   int kind[KMAX], arg[KMAX];
   float sc[KMAX];

@@ -22,15 +22,17 @@ gmm_f32_kernel(const float* __restrict__ A, const float* __restrict__ B0, const 
                const int32_t* __restrict__ off, int N, int Kd, int Nout, int E,
                float* __restrict__ out, float* __restrict__ save) {
   __shared__ int32_t prefix[kMaxExperts + 1];
+  __shared__ int32_t offs[kMaxExperts + 1];
   __shared__ int32_t scratch[32];
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs0[BK][BN + 4];
   __shared__ float Bs1[kSwiglu ? BK : 1][BN + 4];
-  build_tile_prefix(off, E, N, BM, prefix, scratch);
+  stage_offsets(off, E, N, offs, scratch);
+  build_tile_prefix(offs, E, N, BM, prefix, scratch);
   const int tile = blockIdx.x;
   if (tile >= prefix[E]) return;  // uniform across the CTA
   const int e = find_expert(prefix, E, tile);
-  const ExpertRows rows = expert_rows(off, e, N);
+  const ExpertRows rows = expert_rows(offs, e, N);
   const int row0 = rows.lo + (tile - prefix[e]) * BM;
   const int n0 = blockIdx.y * BN;
   const float* b0 = B0 + (size_t)e * Nout * Kd;

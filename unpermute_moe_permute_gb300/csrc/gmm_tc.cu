@@ -843,10 +843,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
   }
   // Every role decodes every tile; the offsets are read from global memory
-  // once here instead of once per tile and role.
-  for (int e = threadIdx.x; e <= p.E; e += blockDim.x)
-    offs[e] = p.off != nullptr ? p.off[e] : (e == 0 ? 0 : p.N);
-  __syncthreads();
+  // once here (sanitised) instead of once per tile and role.
+  stage_offsets(p.off, p.E, p.N, offs, scratch);
   int total;
   if constexpr (Traits<KIND>::wgrad) {
     total = p.E * ((p.m_tiles + CS - 1) / CS) * p.n_tiles;

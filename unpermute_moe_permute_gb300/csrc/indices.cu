@@ -72,15 +72,21 @@ permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E_all, int
   __shared__ int32_t tmp[32];
   __shared__ int32_t s_total;
   __shared__ int32_t s_bad;
+  __shared__ unsigned long long s_sum;  // sum of all counts, in 64 bits
   const int nb = R * E_all, nw = R * C;
-  if (threadIdx.x == 0) s_bad = 0;
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    s_sum = 0ull;
+  }
   __syncthreads();
+  long long my_sum = 0;
   for (int b = threadIdx.x; b < nb; b += kIdxThreads) {
     int c = counts[b];
     if (c < 0) {
       s_bad = 1;
       c = 0;
     }
+    my_sum += c;
     src_rm[b] = c;
     const int r = b / E_all, e = b - r * E_all;
     if (e >= c0 && e < c0 + C) {
@@ -88,7 +94,20 @@ permute_indices_kernel(const int32_t* __restrict__ counts, int R, int E_all, int
       dst_w[(e - c0) * R + r] = c;
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_sum += __shfl_down_sync(0xffffffffu, my_sum, o);
+  if ((threadIdx.x & 31) == 0 && my_sum) atomicAdd(&s_sum, (unsigned long long)my_sum);
   __syncthreads();
+  // The int32 scans below need every prefix sum to fit in int32: a larger
+  // sum is reported as a capacity error and nothing else is written.
+  if (s_sum > 0x7fffffffull) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *total = -1;
+      if (s_bad) set_status(status, MOE_ERR_INVALID_ARG);
+      set_status(status, MOE_ERR_CAPACITY);
+    }
+    return;
+  }
   cta_exclusive_scan(src_rm, nb, tmp, nullptr);
   cta_exclusive_scan(dst_w, nw, tmp, &s_total);
   const int tot = s_total;

@@ -16,7 +16,10 @@
 #include <chrono>
 #include <map>
 #include <mutex>
+#include <random>
 #include <utility>
+
+#include <unistd.h>
 
 #include "common.cuh"
 
@@ -292,7 +295,14 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
   }
   __syncthreads();
   if (timed_out) {
+    // Leave no stale entry behind: this block's slots are not dispatched
+    // (the row copy skips them), and block 0 publishes an empty routing.
     if (tid == 0) set_status(status, MOE_ERR_TIMEOUT);
+    for (int f = b * kChunk + tid; f < min((b + 1) * kChunk, TK); f += kRouteThreads) row_map[f] = -1;
+    if (b == 0) {
+      for (int e = tid; e < E; e += kRouteThreads) tokens_per_expert[e] = 0;
+      for (int e = tid; e <= E; e += kRouteThreads) expert_offsets[e] = 0;
+    }
     return;
   }
   // 4. per expert: total over all blocks and the counts of blocks before b
@@ -372,11 +382,13 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
 }
 
 // One warp per token: read the row once (16-byte vectors), write it to each
-// of its K permuted rows.
+// of its K permuted rows.  Slots whose row lies outside [0, N) (N = rows of
+// the permuted buffer) are skipped: -1 marks a slot that is not dispatched,
+// and nothing else may address memory outside the buffer.
 template <int kUnroll>
 __global__ void __launch_bounds__(256)
 permute_rows_kernel(const uint8_t* __restrict__ tokens, const int32_t* __restrict__ row_map, int T,
-                    int K, int row_bytes, uint8_t* __restrict__ permuted) {
+                    int K, int N, int row_bytes, uint8_t* __restrict__ permuted) {
   // Launched as a programmatic dependent of the routing: wait until that
   // grid has completed and its row_map is visible (a no-op otherwise).
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -398,7 +410,7 @@ permute_rows_kernel(const uint8_t* __restrict__ tokens, const int32_t* __restric
     }
     for (int k = 0; k < K; ++k) {
       const int r = __shfl_sync(0xffffffffu, my_rm, k);
-      if (r < 0) continue;
+      if (r < 0 || r >= N) continue;
       uint8_t* dst = permuted + (size_t)r * row_bytes;
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
@@ -458,11 +470,32 @@ static bool fused_fits(int nblk, int E) {
   return nblk <= it->second;
 }
 
-// A value no earlier call of this process used (and, being seeded from the
-// clock, very unlikely to be found in a fresh workspace).
+// splitmix64 finaliser (Steele, Lea, Flood, "Fast splittable pseudorandom
+// number generators", OOPSLA 2014): spreads every input bit over the output.
+static unsigned long long mix64(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+// A value no earlier call of this process used.  The counter starts from a
+// hash of the clock, the process id and a random_device draw, so a stamp
+// found in a workspace that another process left behind matches only by a
+// 64-bit coincidence; within one process the stamps are unique.
+static unsigned long long stamp_seed() {
+  unsigned long long rd = 0;
+  try {
+    std::random_device dev;
+    rd = ((unsigned long long)dev() << 32) ^ dev();
+  } catch (...) {
+  }
+  const unsigned long long ns =
+      (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+  return mix64(ns ^ mix64((unsigned long long)getpid() ^ mix64(rd)));
+}
+
 static unsigned long long next_stamp() {
-  static std::atomic<unsigned long long> counter{
-      ((unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() << 20) | 1ull};
+  static std::atomic<unsigned long long> counter{stamp_seed()};
   unsigned long long v;
   do {
     v = counter.fetch_add(1ull);
@@ -562,7 +595,8 @@ extern "C" int moe_permute_masked(const void* tokens, int dtype, const int32_t* 
     const uint8_t* tok = static_cast<const uint8_t*>(tokens);
     uint8_t* dst = static_cast<uint8_t*>(permuted);
     const int32_t* rm = row_map;
-    if (cudaLaunchKernelEx(&cfg, permute_rows_kernel<4>, tok, rm, T, K, row_bytes, dst) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, permute_rows_kernel<4>, tok, rm, T, K, TK, row_bytes, dst) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
     count_launches(1);
   }
@@ -578,6 +612,24 @@ extern "C" int moe_permute(const void* tokens, int dtype, const int32_t* expert_
   return moe_permute_masked(tokens, dtype, expert_ids, T, H, K, E, num_special, nullptr, 0,
                             permuted, sorted_indices, row_map, tokens_per_expert, expert_offsets,
                             workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" int moe_permute_rows(const void* tokens, int dtype, const int32_t* row_map, int T, int H,
+                                int K, int N, void* permuted, cudaStream_t stream) {
+  const int esz = dtype_size(dtype);
+  if (esz == 0 || T < 0 || H <= 0 || K <= 0 || N < 0) return MOE_ERR_INVALID_ARG;
+  if (K > kMaxK) return MOE_ERR_SHAPE;
+  if (((size_t)H * esz) % 16 != 0) return MOE_ERR_SHAPE;
+  if ((long long)T * K > 0x7fffffffLL) return MOE_ERR_SHAPE;
+  if (T == 0 || N == 0) return MOE_OK;
+  if (!tokens || !row_map || !permuted) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(tokens) || !aligned16(permuted)) return MOE_ERR_INVALID_ARG;
+  permute_rows_kernel<4><<<(T + 7) / 8, 256, 0, stream>>>(
+      static_cast<const uint8_t*>(tokens), row_map, T, K, N, H * esz,
+      static_cast<uint8_t*>(permuted));
+  count_launches(1);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
 }
 
 extern "C" int moe_invert_sorted_indices(const int32_t* sorted_indices, int N, int TK,
