@@ -15,9 +15,12 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def lib():
-    """The C-ABI library through its Python binding (GPU tests only)."""
+    """The C-ABI library through its Python binding (GPU tests only).  Every
+    call that takes a device status word and is not given one by the test
+    runs with a fresh word that must read MOE_OK afterwards."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from unpermute_moe_permute_gb300 import binding
-    return binding
+    from gpu_util import StatusChecked
+    return StatusChecked(binding)

@@ -3,9 +3,11 @@
 - The bounded waits the tensor-core kernels rely on give up after their limit
   with MOE_ERR_TIMEOUT in the caller's status word, and the context stays
   usable (a library self-test waits on a barrier that nothing arrives on).
-- Corrupt expert offsets made on the host are clamped to the buffer: the
-  grouped GEMMs touch only rows inside the clamped expert ranges, and their
-  results there are those of the oracle on the same ranges.
+- Corrupt expert offsets made on the host are sanitised: clamped to the
+  buffer, then made non-decreasing (each offset raised to the largest one
+  before it), so expert ranges never overlap; the grouped GEMMs touch only
+  rows inside those ranges, and their results there are those of the oracle
+  on the same ranges.
 """
 
 import time
@@ -40,18 +42,20 @@ def test_bounded_wait_times_out_and_context_survives(lib):
     assert np.array_equal(np64(r.expert_offsets), off)
 
 
-# (offsets as given, the ranges they clamp to, first row no range covers)
+# (offsets as given, the sanitised offsets, first row no range covers)
 CORRUPT = [
     ([-5, 40, 30, 30, 25], [0, 40, 40, 40, 40], 40),               # negative, decreasing
     ([-5, 40, 10 ** 9, 10 ** 9, -7], [0, 40, 300, 300, 300], 300),  # past the buffer, negative last
+    ([0, 100, 50, 150, 200], [0, 100, 100, 150, 200], 200),         # would overlap expert 0
 ]
 
 
 @pytest.mark.parametrize("given,clamped,untouched", CORRUPT)
 def test_gemms_clamp_corrupt_offsets(lib, given, clamped, untouched):
-    """Expert e takes rows [lo, hi) with lo = clamp(off[e], 0, N) and
-    hi = clamp(off[e+1], lo, N) over a 300-row buffer; ranges chosen here do
-    not overlap, so the results are the oracle's on the clamped offsets."""
+    """Over a 300-row buffer, offset i becomes max(clamp(off[j], 0, N), j <= i)
+    and expert e takes rows [off[e], off[e+1]): the ranges never overlap, so
+    no two tiles write one row and the results are the oracle's on the
+    sanitised offsets."""
     d = moe_inputs.layer_fwd_bwd(8, T=300, H=128, E=4, K=1, I=64)
     N, H, I = 300, 128, 64
     X = d["tokens"].to(DEV)                               # used as the expert-major rows

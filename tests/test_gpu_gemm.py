@@ -108,6 +108,34 @@ def _sub_forward(perm_rows, experts, d):
     return O.expert_mlp(perm_rows, off, np64(d["W_gate"]), np64(d["W_up"]), np64(d["W_down"]), "bf16")
 
 
+def _token_outputs(d, rm, ts):
+    """Oracle layer output of tokens ts: their K slots' rows through the
+    expert MLP (as a sub-problem grouped by expert) and the unpermute."""
+    K = d["K"]
+    flat = d["expert_ids"].numpy().reshape(-1)
+    slots = (ts[:, None] * K + np.arange(K)).reshape(-1)
+    order = np.argsort(rm[slots], kind="stable")
+    perm_rows = O.permute_rows(np64(d["tokens"]), slots[order], K)
+    _, y, _, _ = _sub_forward(perm_rows, flat[slots[order]], d)
+    sub_rm = np.empty(len(slots), dtype=np.int64)
+    sub_rm[order] = np.arange(len(slots))
+    return O.unpermute(y, sub_rm, d["probs"].numpy()[ts], len(ts), K, "bf16")
+
+
+def _check_sampled_forward(d, si, rm, act, expanded, out, seed, n_rows=600, n_tokens=64):
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(len(si), n_rows, replace=False))
+    flat = d["expert_ids"].numpy().reshape(-1)
+    perm_rows = O.permute_rows(np64(d["tokens"]), si[rows], d["K"])
+    w_act, w_exp, _, _ = _sub_forward(perm_rows, flat[si[rows]], d)
+    sel = torch.from_numpy(rows).to(DEV)
+    assert_normwise(np64(act[sel]), w_act, BF16_TOL, "act rows")
+    assert_normwise(np64(expanded[sel]), w_exp, BF16_TOL, "expanded rows")
+    ts = np.sort(rng.choice(d["T"], n_tokens, replace=False))
+    w_out = _token_outputs(d, rm, ts)
+    assert_normwise(np64(out[torch.from_numpy(ts).to(DEV)]), w_out, BF16_TOL, "layer output rows")
+
+
 def test_bf16_layer_forward_full_size_zipf(lib):
     """T=8192 H=2048 E=256 K=8 I=512, Zipf(1.2) routing with 8 empty experts:
     routing bit-exact, sampled rows of act / expanded / output."""
@@ -120,26 +148,7 @@ def test_bf16_layer_forward_full_size_zipf(lib):
     si, rm, tpe, off = O.permute_routing(d["expert_ids"].numpy(), E)
     assert np.array_equal(np64(r.row_map), rm)
     assert (tpe == 0).sum() == 8
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(len(si), 600, replace=False))
-    flat = d["expert_ids"].numpy().reshape(-1)
-    experts = flat[si[rows]]
-    perm_rows = O.permute_rows(np64(d["tokens"]), si[rows], K)
-    w_act, w_exp, _, _ = _sub_forward(perm_rows, experts, d)
-    sel = torch.from_numpy(rows).to(DEV)
-    assert_normwise(np64(act[sel]), w_act, BF16_TOL, "act rows")
-    assert_normwise(np64(expanded[sel]), w_exp, BF16_TOL, "expanded rows")
-    # output of sampled tokens: their K rows through the oracle
-    ts = np.sort(rng.choice(T, 64, replace=False))
-    slots = (ts[:, None] * K + np.arange(K)).reshape(-1)
-    pos = rm[slots]
-    order = np.argsort(pos, kind="stable")
-    perm_rows = O.permute_rows(np64(d["tokens"]), slots[order], K)
-    _, y, _, _ = _sub_forward(perm_rows, flat[slots[order]], d)
-    sub_rm = np.empty(len(slots), dtype=np.int64)
-    sub_rm[order] = np.arange(len(slots))
-    w_out = O.unpermute(y, sub_rm, d["probs"].numpy()[ts], len(ts), K, "bf16")
-    assert_normwise(np64(out[torch.from_numpy(ts).to(DEV)]), w_out, BF16_TOL, "layer output rows")
+    _check_sampled_forward(d, si, rm, act, expanded, out, seed=0)
 
 
 # ---------------------------------------------------------------- backward
@@ -266,13 +275,15 @@ def test_bf16_mlp_grad_without_rows_writes_zero_weight_grads(lib):
 
 
 def test_bf16_layer_backward_full_size(lib):
-    """T=4096 H=2048 E=128 K=8 I=768 forward + backward: sampled experts'
-    weight grads and rows of d_permuted against the oracle."""
+    """T=4096 H=2048 E=128 K=8 I=768 forward + backward: sampled rows of the
+    forward's act, expanded and layer output, sampled experts' weight grads
+    and rows of d_permuted against the oracle."""
     d = moe_inputs.layer_fwd_bwd(0)
     T, K, E = d["T"], d["K"], d["E"]
     g = _gpu_layer_fwd_bwd(lib, d)
     si, rm, tpe, off = O.permute_routing(d["expert_ids"].numpy(), E)
     assert np.array_equal(np64(g["r"].row_map), rm)
+    _check_sampled_forward(d, si, rm, g["act"], g["expanded"], g["out"], seed=4)
     probs = d["probs"].numpy()
     gout = np64(d["grad_out"])
     tok = np64(d["tokens"])

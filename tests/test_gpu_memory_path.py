@@ -1,9 +1,15 @@
 """GPU parity of the routing and bandwidth kernels against the CPU oracle.
 
-Integer outputs (routing, indices) and copied rows are compared bit for bit;
-floating outputs within the normwise tolerances of tests/gpu_util.py.  Sizes
-span several kernel blocks with ragged tails; the full-size workloads are
-checked on every integer output and on sampled token rows.
+Integer outputs (routing, indices) and copied rows are compared bit for bit.
+Floating outputs are held to what each kernel's arithmetic guarantees: the
+unpermute, the permute backward and the combine accumulate in fp32 and round
+once, so every element must lie within one step of the storage format plus
+the fp32 summation error bound of the oracle's value (assert_elementwise);
+grad_permuted is one fp32 product rounded once, exactly as the oracle rounds
+it, so it is compared bit for bit.  The normwise bars of tests/gpu_util.py
+are kept beside them.  Sizes span several kernel blocks with ragged tails;
+the full-size workloads are checked on every integer output and on sampled
+token rows.
 """
 
 import numpy as np
@@ -12,7 +18,8 @@ import torch
 
 import moe_inputs
 from oracle import moe_oracle as O
-from gpu_util import BF16_TOL, F32_TOL, assert_normwise, np64, tol_for, torch_dtype
+from gpu_util import (BF16_TOL, F32_TOL, assert_bitwise, assert_elementwise, assert_normwise,
+                      np64, tol_for, torch_dtype)
 
 pytestmark = pytest.mark.gpu
 
@@ -170,16 +177,30 @@ def test_unpermute_and_grads(lib, dtype, T, K, E, H, special):
     r = lib.moe_permute(None, ids.to(DEV), E, special)
     assert np.array_equal(np64(r.row_map), rm)
     ex_d = expanded.to(DEV).contiguous()
+    Y, G, p = np64(expanded), np64(grad_out), probs.numpy()
     out = lib.moe_unpermute(ex_d, r.row_map, probs.to(DEV), T, K)
-    assert_normwise(np64(out), O.unpermute(np64(expanded), rm, probs.numpy(), T, K, dtype), tol, "unpermute")
+    want = O.unpermute(Y, rm, p, T, K, dtype)
+    assert_normwise(np64(out), want, tol, "unpermute")
+    mag = O.unpermute(np.abs(Y), rm, np.abs(p), T, K, "f64")
+    assert_elementwise(np64(out), want, mag, K, dtype, "unpermute")
     out1 = lib.moe_unpermute(ex_d, r.row_map, None, T, K)
-    assert_normwise(np64(out1), O.unpermute(np64(expanded), rm, None, T, K, dtype), tol, "unpermute p=1")
+    want = O.unpermute(Y, rm, None, T, K, dtype)
+    assert_normwise(np64(out1), want, tol, "unpermute p=1")
+    assert_elementwise(np64(out1), want, O.unpermute(np.abs(Y), rm, None, T, K, "f64"), K, dtype,
+                       "unpermute p=1")
     gp, gprob = lib.moe_unpermute_grad(grad_out.to(DEV), ex_d, r.row_map, probs.to(DEV), K)
-    w_gp, w_gprob = O.unpermute_grad(np64(grad_out), np64(expanded), rm, probs.numpy(), T, K, dtype)
+    w_gp, w_gprob = O.unpermute_grad(G, Y, rm, p, T, K, dtype)
     assert_normwise(np64(gp), w_gp, tol, "grad_permuted")
+    assert_bitwise(np64(gp), w_gp, "grad_permuted")
     assert_normwise(np64(gprob), w_gprob, F32_TOL, "grad_probs")
+    # each lane chains H/32 fp32 FMAs, then five shuffle additions
+    _, mag_p = O.unpermute_grad(np.abs(G), np.abs(Y), rm, None, T, K, "f64")
+    assert_elementwise(np64(gprob), w_gprob, mag_p, H // 32 + 5, "f32", "grad_probs")
     gt = lib.moe_permute_grad(ex_d, r.row_map, T, K)
-    assert_normwise(np64(gt), O.permute_grad(np64(expanded), rm, T, K, dtype), tol, "permute_grad")
+    want = O.permute_grad(Y, rm, T, K, dtype)
+    assert_normwise(np64(gt), want, tol, "permute_grad")
+    assert_elementwise(np64(gt), want, O.permute_grad(np.abs(Y), rm, T, K, "f64"), K, dtype,
+                       "permute_grad")
 
 
 def test_unpermute_k1_roundtrip_is_identity(lib):
@@ -204,6 +225,21 @@ def test_invert_sorted_indices(lib):
 
 # ---------------------------------------------------------------- combine
 
+def _combine_mag(expanded, rm, ids, scales, shared_x, ori_x, E, Z, C, Cn, a1, a2, v,
+                 active_mask=None):
+    """Per element, the sum of the absolute values of the combine's terms:
+    the oracle's combine of the inputs' absolute values, unrounded."""
+    ab = lambda x: None if x is None else np.abs(x)  # noqa: E731
+    return O.combine(ab(expanded), rm, ids, ab(scales), ab(shared_x), ab(ori_x), E, Z, C, Cn,
+                     ab(a1), ab(a2), ab(v), "f64", active_mask=active_mask)
+
+
+def _combine_roundings(K):
+    # per slot: a const expert's two fp32 operations and the FMA into the sum;
+    # then the shared-expert addition
+    return 3 * K + 1
+
+
 @pytest.mark.parametrize("T,K,E,H,Z,C,Cn,shared", [
     (37, 4, 16, 64, 1, 1, 1, True),
     (500, 8, 64, 264, 4, 4, 4, True),
@@ -226,10 +262,13 @@ def test_combine(lib, T, K, E, H, Z, C, Cn, shared):
                           zero_num=Z, copy_num=C, const_num=Cn, alpha1=d["alpha1"].to(DEV),
                           alpha2=d["alpha2"].to(DEV), const_v=d["const_v"].to(DEV), dev_status=st)
     assert lib.moe_check_status(st) == lib.MOE_OK
-    want = O.combine(np64(d["expanded"]), rm, ids.numpy(), d["scales"].numpy(),
-                     np64(sx) if shared else None, np64(d["ori_x"]), E, Z, C, Cn,
-                     np64(d["alpha1"]), np64(d["alpha2"]), np64(d["const_v"]), "bf16")
+    args = (np64(d["expanded"]), rm, ids.numpy(), d["scales"].numpy(),
+            np64(sx) if shared else None, np64(d["ori_x"]), E, Z, C, Cn,
+            np64(d["alpha1"]), np64(d["alpha2"]), np64(d["const_v"]))
+    want = O.combine(*args, "bf16")
     assert_normwise(np64(out), want, BF16_TOL, "combine")
+    assert_elementwise(np64(out), want, _combine_mag(*args), _combine_roundings(K), "bf16",
+                       "combine")
 
 
 def test_combine_page_example_ids(lib):
@@ -252,14 +291,17 @@ def test_combine_page_example_ids(lib):
     out = lib.moe_combine(expanded.to(DEV), r.row_map, ids.to(DEV), s.to(DEV), E, ori_x=ori.to(DEV),
                           zero_num=1, copy_num=1, const_num=1, alpha1=a1.to(DEV), alpha2=a2.to(DEV),
                           const_v=v.to(DEV))
-    want = O.combine(np64(expanded), rm, ids.numpy(), s.numpy(), None, np64(ori), E, 1, 1, 1,
-                     np64(a1), np64(a2), np64(v), "bf16")
+    args = (np64(expanded), rm, ids.numpy(), s.numpy(), None, np64(ori), E, 1, 1, 1,
+            np64(a1), np64(a2), np64(v))
+    want = O.combine(*args, "bf16")
     assert_normwise(np64(out), want, BF16_TOL, "combine page example")
+    assert_elementwise(np64(out), want, _combine_mag(*args), _combine_roundings(K), "bf16",
+                       "combine page example")
 
 
 def test_combine_reports_ids_past_special_ranges(lib):
     ids = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32)
-    r = lib.moe_permute(None, ids.to(DEV), 4, 5)        # routing accepts id 9 < 4 + 5
+    r = lib.moe_permute(None, ids.to(DEV), 4, 6)        # routing accepts id 9 < 4 + 6
     st = lib.new_status()
     lib.moe_combine(torch.zeros((3, 64), dtype=torch.bfloat16, device=DEV), r.row_map,
                     ids.to(DEV), torch.ones((2, 2), device=DEV), 4, ori_x=torch.zeros((2, 64), dtype=torch.bfloat16, device=DEV),
@@ -293,6 +335,52 @@ def test_permute_indices_capacity_overflow(lib):
     assert torch.all(idx == -7)                  # nothing written past the check
 
 
+def test_permute_indices_sum_past_int32(lib):
+    """Counts whose sum passes 2^31 - 1 (four of 2^30 - 1, and one more): the
+    64-bit check reports a capacity error, sets total = -1 and writes no
+    index or count."""
+    counts = torch.tensor([2 ** 30 - 1] * 4 + [3], dtype=torch.int32)
+    assert int(counts.sum(dtype=torch.int64)) > 2 ** 31 - 1
+    idx = torch.full((64,), -7, dtype=torch.int32, device=DEV)
+    tpe = torch.full((5,), -7, dtype=torch.int32, device=DEV)
+    st = lib.new_status()
+    _, _, total = lib.moe_permute_indices(counts.to(DEV), 1, 5, 64, indices=idx,
+                                          tokens_per_expert=tpe, dev_status=st)
+    assert lib.moe_check_status(st) == lib.MOE_ERR_CAPACITY
+    assert int(total.item()) == -1
+    assert torch.all(idx == -7) and torch.all(tpe == -7)
+
+
+# ---------------------------------------------------------------- row copy with a given routing
+
+def test_permute_rows_skips_rows_outside_the_buffer(lib):
+    """moe_permute_rows copies token rows to the rows row_map names, and
+    skips every entry outside [0, N): -1, N, large and negative values made
+    on the host leave the buffer untouched; valid entries are exact copies."""
+    T, K, H, N = 40, 3, 64, 100
+    rng = np.random.default_rng(5)
+    tok = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).bfloat16()
+    rm = np.full(T * K, -1, dtype=np.int64)
+    valid = rng.choice(T * K, 60, replace=False)
+    rm[valid] = rng.choice(N - 10, 60, replace=False)      # rows [0, 90) only
+    junk = np.setdiff1d(np.arange(T * K), valid)
+    rm[junk[0::4]] = N
+    rm[junk[1::4]] = N + 12345
+    rm[junk[2::4]] = 2 ** 31 - 1
+    rm[junk[3::4]] = -(2 ** 31)
+    sentinel = 3.0
+    out = torch.full((N + 16, H), sentinel, dtype=torch.bfloat16, device=DEV)  # 16 rows past N
+    lib.moe_permute_rows(tok.to(DEV), torch.from_numpy(rm.astype(np.int32)).to(DEV), K, N,
+                         permuted=out)
+    torch.cuda.synchronize()
+    got = np64(out)
+    assert np.all(got[N:] == sentinel)
+    written = np.zeros(N + 16, dtype=bool)
+    written[rm[valid]] = True
+    assert np.all(got[~written] == sentinel)
+    assert np.array_equal(got[rm[valid]], np64(tok)[valid // K])
+
+
 # ---------------------------------------------------------------- full-size workloads (sampled)
 
 def _sample(n, k, seed):
@@ -322,15 +410,25 @@ def test_permute_unpermute_full_size_bf16(lib):
     # sub-problem of the sampled tokens: their K oracle-permuted rows
     sub_rows = O.permute_rows(np64(tok), slots, K)
     sub_rm = np.arange(len(slots))
-    w_out = O.unpermute(sub_rows, sub_rm, probs.numpy()[ts], len(ts), K, "bf16")
-    assert_normwise(np64(out[torch.from_numpy(ts).to(DEV)]), w_out, BF16_TOL, "unpermute full")
-    w_gp, w_gprob = O.unpermute_grad(np64(gout)[ts], sub_rows, sub_rm, probs.numpy()[ts], len(ts), K, "bf16")
+    p_s, g_s = probs.numpy()[ts], np64(gout)[ts]
+    w_out = O.unpermute(sub_rows, sub_rm, p_s, len(ts), K, "bf16")
+    got_out = np64(out[torch.from_numpy(ts).to(DEV)])
+    assert_normwise(got_out, w_out, BF16_TOL, "unpermute full")
+    assert_elementwise(got_out, w_out, O.unpermute(np.abs(sub_rows), sub_rm, np.abs(p_s), len(ts), K, "f64"),
+                       K, "bf16", "unpermute full")
+    w_gp, w_gprob = O.unpermute_grad(g_s, sub_rows, sub_rm, p_s, len(ts), K, "bf16")
     got_gp = np64(gp[torch.from_numpy(rm[slots]).to(DEV)])
     assert_normwise(got_gp, w_gp, BF16_TOL, "grad_permuted full")
+    assert_bitwise(got_gp, w_gp, "grad_permuted full")
     assert_normwise(np64(gprob)[ts], w_gprob, F32_TOL, "grad_probs full")
+    _, mag_p = O.unpermute_grad(np.abs(g_s), np.abs(sub_rows), sub_rm, None, len(ts), K, "f64")
+    assert_elementwise(np64(gprob)[ts], w_gprob, mag_p, H // 32 + 5, "f32", "grad_probs full")
     gt = lib.moe_permute_grad(gp, r.row_map, T, K)
     w_gt = O.permute_grad(w_gp, sub_rm, len(ts), K, "bf16")
-    assert_normwise(np64(gt[torch.from_numpy(ts).to(DEV)]), w_gt, BF16_TOL, "permute_grad full")
+    got_gt = np64(gt[torch.from_numpy(ts).to(DEV)])
+    assert_normwise(got_gt, w_gt, BF16_TOL, "permute_grad full")
+    assert_elementwise(got_gt, w_gt, O.permute_grad(np.abs(w_gp), sub_rm, len(ts), K, "f64"), K,
+                       "bf16", "permute_grad full")
 
 
 def test_index_and_combine_full_size(lib):
@@ -352,10 +450,13 @@ def test_index_and_combine_full_size(lib):
                           shared_x=d["shared_x"].to(DEV), ori_x=d["ori_x"].to(DEV), zero_num=Z,
                           copy_num=C, const_num=Cn, alpha1=d["alpha1"].to(DEV),
                           alpha2=d["alpha2"].to(DEV), const_v=d["const_v"].to(DEV))
-    want = O.combine(np64(d["expanded"]), rm, ids.numpy(), d["scales"].numpy(), np64(d["shared_x"]),
-                     np64(d["ori_x"]), E, Z, C, Cn, np64(d["alpha1"]), np64(d["alpha2"]),
-                     np64(d["const_v"]), "bf16")
+    args = (np64(d["expanded"]), rm, ids.numpy(), d["scales"].numpy(), np64(d["shared_x"]),
+            np64(d["ori_x"]), E, Z, C, Cn, np64(d["alpha1"]), np64(d["alpha2"]),
+            np64(d["const_v"]))
+    want = O.combine(*args, "bf16")
     assert_normwise(np64(out), want, BF16_TOL, "combine full")
+    assert_elementwise(np64(out), want, _combine_mag(*args), _combine_roundings(d["K"]), "bf16",
+                       "combine full")
 
 
 # ---------------------------------------------------------------- deredundancy indices
@@ -375,6 +476,32 @@ def test_deredundancy_indices_bit_exact(lib, nsrc, NE, start, D, L, lam):
     assert int(total.item()) == want_total
     assert np.array_equal(np64(idx)[:want_total], want_idx)
     assert np.array_equal(np64(n)[:D * L], want_n)
+
+
+@pytest.mark.parametrize("nsrc,NE,start,D,L,H", [(4, 32, 8, 2, 4, 64), (16, 128, 0, 4, 8, 2048),
+                                                 (3, 10, 9, 1, 1, 8)])
+def test_whiteboard_combine_of_the_deredundancy_dispatch(lib, nsrc, NE, start, D, L, H):
+    """The deredundancy dispatcher's combine (scale each expert output row by
+    its router coefficient, scatter-add it to its gathered row of a zero
+    whiteboard) on one outer-EP rank, as this library runs it: the dispatch
+    indices of moe_permute_indices_window, inverted into a row map by
+    moe_invert_sorted_indices, and the unpermute with one slot per gathered
+    row weighted by its coefficient.  Each whiteboard row is at most one
+    product rounded once, so it matches the oracle bit for bit."""
+    rng = np.random.Generator(np.random.PCG64(nsrc * 7 + NE + H))
+    counts = rng.poisson(6.0, size=(nsrc, NE)).astype(np.int32)
+    n_gathered = int(counts.sum())
+    want_idx, _, n = O.deredundancy_dispatch_indices(counts, start, D, L)
+    Y = torch.from_numpy(rng.standard_normal((max(n, 1), H)).astype(np.float32)).bfloat16()[:n]
+    coeff = torch.from_numpy(rng.random(n_gathered).astype(np.float32))
+    idx, _, total = lib.moe_permute_indices_window(torch.from_numpy(counts.reshape(-1)).to(DEV),
+                                                   nsrc, NE, start, D * L, max(n, 1))
+    assert int(total.item()) == n
+    rm = lib.moe_invert_sorted_indices(idx, n, n_gathered)
+    wb = lib.moe_unpermute(Y.to(DEV).contiguous(), rm, coeff.reshape(n_gathered, 1).to(DEV),
+                           n_gathered, 1)
+    want = O.whiteboard_combine(np64(Y), want_idx, coeff.numpy(), n_gathered, "bf16")
+    assert_bitwise(np64(wb), want, "whiteboard")
 
 
 def test_full_window_equals_permute_indices(lib):
@@ -409,7 +536,40 @@ def test_masked_permute_and_combine(lib, dims):
                           copy_num=2, const_num=2, alpha1=d["alpha1"].to(DEV),
                           alpha2=d["alpha2"].to(DEV), const_v=d["const_v"].to(DEV),
                           active_mask=mask_t)
-    want = O.combine(np64(expanded), rm, ids.numpy(), d["scales"].numpy(), np64(d["shared_x"]),
-                     np64(d["ori_x"]), E, 2, 2, 2, np64(d["alpha1"]), np64(d["alpha2"]),
-                     np64(d["const_v"]), "bf16", active_mask=mask)
+    args = (np64(expanded), rm, ids.numpy(), d["scales"].numpy(), np64(d["shared_x"]),
+            np64(d["ori_x"]), E, 2, 2, 2, np64(d["alpha1"]), np64(d["alpha2"]),
+            np64(d["const_v"]))
+    want = O.combine(*args, "bf16", active_mask=mask)
     assert_normwise(np64(out), want, BF16_TOL, "masked combine")
+    assert_elementwise(np64(out), want, _combine_mag(*args, active_mask=mask),
+                       _combine_roundings(K), "bf16", "masked combine")
+
+
+@pytest.mark.parametrize("dims", [1, 2])
+def test_masked_combine_still_validates_ids(lib, dims):
+    """A masked-off slot is not read, but its id must still name an expert:
+    an id past the special ranges on a masked slot is reported; routed ids
+    on masked slots (row_map -1 after the masked permute) are not."""
+    T, K, E, H = 64, 4, 16, 64
+    rng = np.random.Generator(np.random.PCG64(40 + dims))
+    ids = moe_inputs.uniform_distinct_ids(rng, T, K, E + 3)
+    mask = np.ones(T, dtype=bool) if dims == 1 else np.ones((T, K), dtype=bool)
+    mask[5] = False                                      # token 5 (all its slots) masked off
+    mask_t = torch.from_numpy(mask).to(DEV)
+    r = lib.moe_permute(None, ids.to(DEV), E, 3, active_mask=mask_t)
+    n = int(r.expert_offsets[-1].item())
+    expanded = torch.randn((max(n, 1), H), device=DEV).bfloat16()
+    ori = torch.randn((T, H), device=DEV).bfloat16()
+    a = torch.ones((1, H), dtype=torch.bfloat16, device=DEV)
+    kw = dict(ori_x=ori, zero_num=1, copy_num=1, const_num=1, alpha1=a, alpha2=a, const_v=a,
+              active_mask=mask_t)
+    st = lib.new_status()
+    lib.moe_combine(expanded, r.row_map, ids.to(DEV), torch.ones((T, K), device=DEV), E,
+                    dev_status=st, **kw)
+    assert lib.moe_check_status(st) == lib.MOE_OK
+    bad = ids.clone()
+    bad[5, 2] = E + 3                                    # past the special ranges, masked slot
+    st = lib.new_status()
+    lib.moe_combine(expanded, r.row_map, bad.to(DEV), torch.ones((T, K), device=DEV), E,
+                    dev_status=st, **kw)
+    assert lib.moe_check_status(st) == lib.MOE_ERR_BAD_ID

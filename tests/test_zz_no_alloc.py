@@ -1,4 +1,5 @@
-"""The allocation-free permute entry point against the workspace one.
+"""The allocation-free permute entry point against the workspace one and
+against the oracle.
 
 moe_permute_static_scratch serves callers that cannot allocate device memory
 (a plugin given only its input and output buffers, or a process whose device
@@ -13,6 +14,7 @@ import pytest
 import torch
 
 import moe_inputs
+from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +43,15 @@ def test_static_scratch_permute_matches_workspace_permute_on_consecutive_calls(l
         n = int(ref.expert_offsets[-1].item())
         assert torch.equal(got.sorted_indices[:n], ref.sorted_indices[:n])
         assert torch.equal(got.permuted[:n], ref.permuted[:n])
+        # and bit for bit against the oracle's routing and row gather
+        si, rm, tpe, off = O.permute_routing(ids.cpu().numpy(), E, special)
+        assert n == len(si)
+        assert np.array_equal(got.expert_offsets.cpu().numpy(), off)
+        assert np.array_equal(got.tokens_per_expert.cpu().numpy(), tpe)
+        assert np.array_equal(got.row_map.cpu().numpy(), rm)
+        assert np.array_equal(got.sorted_indices[:n].cpu().numpy(), si)
+        want = O.permute_rows(tok.float().cpu().numpy().astype(np.float64), si, K)
+        assert np.array_equal(got.permuted[:n].float().cpu().numpy().astype(np.float64), want)
 
 
 def test_static_scratch_permute_rejects_sizes_past_its_array(lib):
