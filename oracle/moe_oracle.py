@@ -28,7 +28,7 @@ Sources (cited by page title and section):
         + SwiGLU on stacked expert weights; ``permute`` as ``x[idx]`` whose
         backward accumulates duplicate indices.
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
   R1 unpermute forward = probability-weighted gather-sum over the K slots.
   R2 ``sorted_indices`` uses the gather convention of [EP]: entry i is the
      flat slot f = t*K + k whose row lands at permuted row i.
@@ -67,6 +67,9 @@ __all__ = [
     "combine",
     "permute_indices",
     "deredundancy_dispatch_indices",
+    "scale_by_router_coeff",
+    "scatter_add_first_dim",
+    "whiteboard_combine",
     "permute_grad",
     "expert_mlp_grad",
 ]
@@ -426,6 +429,52 @@ def deredundancy_dispatch_indices(counts, expert_start: int, iep_size: int,
                 n += int(c[o, e])
             per_dest_expert.append(n)
     return np.array(out, dtype=np.int64), np.array(per_dest_expert, dtype=np.int64), len(out)
+
+
+# --------------------------------------------------------------------------
+# The deredundancy dispatcher's combine ([EP] _scale_by_router_coeff,
+# _scatter_add_first_dim and the combine that calls them)
+# --------------------------------------------------------------------------
+
+def scale_by_router_coeff(rows, router_coeff):
+    """[EP] ``_scale_by_router_coeff``: each routed expert-output row times
+    its own router coefficient; no coefficients leave the rows unchanged.
+    The coefficient vector must have one entry per row (ValueError
+    otherwise)."""
+    Y = np.asarray(rows, dtype=np.float64)
+    if router_coeff is None:
+        return Y
+    c = np.asarray(router_coeff, dtype=np.float64).reshape(-1)
+    if c.shape[0] != Y.shape[0]:
+        raise ValueError("router_coeff length must match the number of routed rows")
+    return Y * c.reshape((-1,) + (1,) * (Y.ndim - 1))
+
+
+def scatter_add_first_dim(src, indices, n_rows: int):
+    """[EP] ``_scatter_add_first_dim``: a zero buffer of ``n_rows`` rows to
+    which row i of ``src`` is added at row ``indices[i]`` (rows named more
+    than once accumulate)."""
+    S = np.asarray(src, dtype=np.float64)
+    out = np.zeros((int(n_rows),) + S.shape[1:])
+    for i, j in enumerate(np.asarray(indices, dtype=np.int64).reshape(-1)):
+        out[j] += S[i]
+    return out
+
+
+def whiteboard_combine(expert_rows, dispatch_indices, gathered_coeff, n_gathered: int,
+                       dtype: str):
+    """The deredundancy combine on one outer-EP rank ([EP], the combine of
+    the deredundancy dispatcher with an outer-EP size of 1, so no
+    reduce-scatter follows): the dispatch gathered rows ``dispatch_indices``
+    of the gathered buffer (with their router coefficients
+    ``gathered_coeff[dispatch_indices]``); the combine scales the expert
+    outputs of those rows by their coefficients and scatter-adds them back to
+    the same positions of a zero [n_gathered, H] whiteboard, in that order.
+    ``gathered_coeff`` None means no scaling."""
+    idx = np.asarray(dispatch_indices, dtype=np.int64).reshape(-1)
+    coeff = None if gathered_coeff is None else np.asarray(gathered_coeff, dtype=np.float64)[idx]
+    weighted = scale_by_router_coeff(expert_rows, coeff)
+    return round_to(scatter_add_first_dim(weighted, idx, n_gathered), dtype)
 
 
 # --------------------------------------------------------------------------

@@ -604,3 +604,126 @@ def test_masked_combine_equals_zero_scale():
     got = O.combine(Y, rm, ids, s, sh, ori, E, 1, 1, 1, a1, a2, v, "f64", active_mask=mask)
     want = O.combine(Y, rm, ids, np.where(mask, s, 0.0), sh, ori, E, 1, 1, 1, a1, a2, v, "f64")
     assert np.allclose(got, want, atol=1e-14)
+
+
+# ---------------------------------------------------------------- bf16 storage rounding of the MLP
+
+def _tbf16(t):
+    """torch's own float32 -> bfloat16 conversion (round to nearest even),
+    back to float64: an implementation of the storage rounding that shares
+    nothing with the oracle's round_to_bf16."""
+    return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+
+def _mlp_case(seed, E=3, H=16, I=24, rows=(5, 0, 9)):
+    rng = np.random.default_rng(seed)
+    off = np.concatenate([[0], np.cumsum(rows)])
+    X = O.round_to_bf16(rng.standard_normal((int(off[-1]), H)))
+    Wg = O.round_to_bf16(rng.standard_normal((E, I, H)) * 0.3)
+    Wu = O.round_to_bf16(rng.standard_normal((E, I, H)) * 0.3)
+    Wd = O.round_to_bf16(rng.standard_normal((E, H, I)) * 0.3)
+    return off, X, Wg, Wu, Wd
+
+
+def test_expert_mlp_bf16_rounds_exactly_act_and_expanded():
+    """The "bf16" branch of expert_mlp rounds the stored tensors, act before
+    the down projection and the expanded output, and nothing else (reading
+    R7): a per-expert loop in torch float64 that rounds with torch's bf16
+    conversion at those two points gives the same bits.  Dropping the act
+    rounding changes the output, so the pin sees that rounding point."""
+    off, X, Wg, Wu, Wd = _mlp_case(21)
+    act, out, g, u = O.expert_mlp(X, off, Wg, Wu, Wd, "bf16")
+    tX = torch.from_numpy(X)
+    for e in range(len(off) - 1):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if lo == hi:
+            continue
+        tg = tX[lo:hi] @ torch.from_numpy(Wg[e]).T
+        tu = tX[lo:hi] @ torch.from_numpy(Wu[e]).T
+        ta = _tbf16(torch.nn.functional.silu(tg) * tu)
+        ty = _tbf16(ta @ torch.from_numpy(Wd[e]).T)
+        assert np.array_equal(act[lo:hi], ta.numpy())
+        assert np.array_equal(out[lo:hi], ty.numpy())
+        assert np.allclose(g[lo:hi], tg.numpy(), rtol=1e-14, atol=0)     # unrounded
+        unrounded_act = _tbf16((torch.nn.functional.silu(tg) * tu) @ torch.from_numpy(Wd[e]).T)
+        assert not np.array_equal(out[lo:hi], unrounded_act.numpy())
+
+
+def test_expert_mlp_grad_bf16_rounds_exactly_the_stored_gradients():
+    """The "bf16" branch of expert_mlp_grad rounds dg and du (stored between
+    the down dgrad and the gate/up GEMMs), d_permuted and the three weight
+    gradients, and nothing else: the same chain rule in torch float64 with
+    torch's bf16 conversion at those points gives the same bits.  Feeding the
+    unrounded dg, du to the gate/up dgrad changes d_permuted, so the pin sees
+    that rounding point."""
+    off, X, Wg, Wu, Wd = _mlp_case(22)
+    rng = np.random.default_rng(23)
+    act, _, _, _ = O.expert_mlp(X, off, Wg, Wu, Wd, "bf16")
+    dY = O.round_to_bf16(rng.standard_normal((X.shape[0], X.shape[1])))
+    dX, dWg, dWu, dWd = O.expert_mlp_grad(dY, X, act, off, Wg, Wu, Wd, "bf16")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))  # noqa: E731
+    for e in range(len(off) - 1):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if lo == hi:
+            assert not dWg[e].any() and not dWu[e].any() and not dWd[e].any()
+            continue
+        x, dy, a = t(X[lo:hi]), t(dY[lo:hi]), t(act[lo:hi])
+        g, u = x @ t(Wg[e]).T, x @ t(Wu[e]).T
+        s = torch.sigmoid(g)
+        dA = dy @ t(Wd[e])
+        dg_raw = dA * u * s * (1 + g * (1 - s))
+        du_raw = dA * torch.nn.functional.silu(g)
+        dg, du = _tbf16(dg_raw), _tbf16(du_raw)
+        assert np.array_equal(dX[lo:hi], _tbf16(dg @ t(Wg[e]) + du @ t(Wu[e])).numpy())
+        assert np.array_equal(dWd[e], _tbf16(dy.T @ a).numpy())
+        assert np.array_equal(dWg[e], _tbf16(dg.T @ x).numpy())
+        assert np.array_equal(dWu[e], _tbf16(du.T @ x).numpy())
+        unrounded = _tbf16(dg_raw @ t(Wg[e]) + du_raw @ t(Wu[e])).numpy()
+        assert not np.array_equal(dX[lo:hi], unrounded)
+
+
+# ---------------------------------------------------------------- whiteboard combine
+
+def test_whiteboard_combine_hand_case():
+    """Three dispatched rows of a five-row gathered buffer, worked by hand:
+    row i of the expert outputs is scaled by the coefficient of gathered row
+    d[i] and lands at row d[i]; the other rows stay zero."""
+    rows = np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0]])
+    d = np.array([4, 0, 2])
+    coeff = np.array([0.5, 9.0, -1.0, 9.0, 2.0])        # per gathered row
+    want = np.array([[1.5, 2.0], [0.0, 0.0], [-5.0, -6.0], [0.0, 0.0], [2.0, 4.0]])
+    assert np.array_equal(O.whiteboard_combine(rows, d, coeff, 5, "f64"), want)
+    assert np.array_equal(O.whiteboard_combine(rows, d, None, 5, "f64")[4], [1.0, 2.0])
+
+
+def test_scatter_add_first_dim_accumulates_repeated_rows():
+    src = np.array([[1.0], [2.0], [4.0], [8.0]])
+    got = O.scatter_add_first_dim(src, np.array([1, 3, 1, 1]), 4)
+    assert np.array_equal(got, [[0.0], [13.0], [0.0], [2.0]])
+
+
+def test_scale_by_router_coeff_rules():
+    rows = np.arange(6.0).reshape(3, 2)
+    assert np.array_equal(O.scale_by_router_coeff(rows, None), rows)
+    assert np.array_equal(O.scale_by_router_coeff(rows, [1.0, -2.0, 0.5]),
+                          [[0.0, 1.0], [-4.0, -6.0], [2.0, 2.5]])
+    with pytest.raises(ValueError):
+        O.scale_by_router_coeff(rows, [1.0, 2.0])
+
+
+def test_whiteboard_combine_on_dispatch_indices_is_the_k1_unpermute():
+    """On the deredundancy dispatch indices (distinct rows of the gathered
+    buffer) the scatter-add whiteboard equals the weighted gather of the
+    unpermute with one slot per gathered row, weight = its coefficient and
+    row_map = the inverse of the dispatch indices (-1 for rows not
+    dispatched)."""
+    rng = np.random.default_rng(24)
+    counts = rng.poisson(3.0, size=(4, 12))
+    idx, _, n = O.deredundancy_dispatch_indices(counts, 4, 2, 3)
+    total = int(counts.sum())
+    Y = rng.standard_normal((n, 5))
+    coeff = rng.random(total)
+    wb = O.whiteboard_combine(Y, idx, coeff, total, "f64")
+    rm = np.full(total, -1)
+    rm[idx] = np.arange(n)
+    assert np.allclose(wb, O.unpermute(Y, rm, coeff.reshape(total, 1), total, 1, "f64"), atol=0)
