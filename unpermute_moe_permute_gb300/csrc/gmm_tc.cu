@@ -15,7 +15,9 @@
 //     columns) drain an accumulator with tcgen05.ld while the next tile
 //     accumulates into the other one, apply the epilogue, stage bf16 in
 //     shared memory and write it with TMA stores;
-//   * the wgrads add a warp that zeroes expert tail rows in shared memory;
+//   * the wgrads reduce over each expert's own rows: the last, partial k
+//     block of an expert is loaded through a tensor map that zero-fills the
+//     rows past the expert's end (see the wgrad tail below);
 //   * gate/up, down and the gate/up dgrad also come as CTA pairs (tcgen05
 //     cta_group::2, a 2-CTA cluster on one TPC, M=256 per MMA, half of the
 //     B tile per CTA, 6-stage ring; an expert's last <= 128 rows as an M=128
@@ -77,10 +79,8 @@ struct Traits {
   static constexpr bool a_mn = (kind_of(KIND) == kWgradDown || kind_of(KIND) == kWgradGateUp);
   static constexpr bool b_mn = (kind_of(KIND) >= kDgradDown);
   static constexpr bool wgrad = (kind_of(KIND) == kWgradDown || kind_of(KIND) == kWgradGateUp);
-  // TMA producer, MMA issuer, epilogue warps, and for the wgrads one warp
-  // that zeroes the rows past an expert's end in its last k block, so that
-  // the MMA-issuing warp only issues.
-  static constexpr int threads = 64 + 32 * kEpiWarps + (wgrad ? 32 : 0);
+  // TMA producer, MMA issuer, epilogue warps.
+  static constexpr int threads = 64 + 32 * kEpiWarps;
   // UMMA N (256 for every kind; a 192-wide down-dgrad tile, which evens out
   // its waves at I = 768, measured slower because that kernel is bound by
   // its epilogue, not by idle SMs).
@@ -94,12 +94,8 @@ struct Traits {
   // ring.  When at most 128 of an expert's rows are left, the pair takes
   // them as a half tile (M=128 over the pair, 64 rows per CTA), so pairs
   // cover the same rows as single CTAs.  Whether a call runs paired
-  // is decided per call and kind from the rows per expert (use_pairs).  The
-  // wgrads stay single: their expert tail rows are zeroed in shared memory
-  // after the loads land, which the leader cannot observe for the peer's
-  // loads.
+  // is decided per call and kind from the rows per expert (use_pairs).
   static constexpr bool pair = (KIND & kPaired) != 0;
-  static_assert(!(pair && wgrad), "the wgrad tail fix-up is single-CTA");
   static constexpr int cs = pair ? 2 : 1;  // CTAs per cluster
   static constexpr int b_rows = pair ? bn / 2 : bn;  // B rows (N) this CTA holds
   static constexpr uint32_t idesc = idesc_bf16_f32(BM * cs, bn, a_mn, b_mn);
@@ -198,24 +194,22 @@ __device__ __forceinline__ Waves plan_waves(int total, int grid) {
   return w;
 }
 
-// Wgrad k block kb of tile x (k = the expert's token rows): the MMAs cover
-// nk 16-row groups; rows [z0, z0 + zl) of the block lie inside the last of
-// them but belong to the next expert and must read as zero.
-struct KTail {
-  int nk, z0, zl;
-};
-
+// Wgrad tail.  The wgrads reduce over an expert's token rows (k), and the
+// rows after the expert's end belong to the next expert: the last, partial
+// k block of an expert must read them as zero.  Both operands are loaded
+// through 3-D tensor maps whose dimensions 1 and 2 both step one row
+// (element (c, i, j) is row i + j, dimension 1 of extent bk): a k block at
+// row r0 = lo + kb * bk with rem = hi - r0 < bk valid rows is loaded at
+// (c, rem - bk, r0), so that box row q holds row r0 + q - (bk - rem), and
+// its first bk - rem rows, whose dimension-1 coordinates are negative, are
+// zero-filled by the TMA unit.  A and B are shifted alike, so the k sum is
+// that of the expert's rows alone; the MMAs skip the leading groups of 16
+// rows that are all zero.  Full blocks load at (c, 0, r0).
 template <int KIND>
-__device__ __forceinline__ KTail k_tail(const Tile& x, int kb) {
+__device__ __forceinline__ int k_shift(const Tile& x, int kb) {
   constexpr int BK = Traits<KIND>::bk;
   const int rem = x.hi - (x.lo + kb * BK);
-  KTail r{BK / UK, BK, 0};
-  if (rem < BK) {
-    r.nk = (rem + UK - 1) / UK;
-    r.z0 = rem;
-    r.zl = r.nk * UK - rem;
-  }
-  return r;
+  return rem < BK ? BK - rem : 0;
 }
 
 // Tile t: a group of CS (1, or 2 for a pair) vertically adjacent 128-row tiles of one
@@ -334,10 +328,11 @@ __device__ __forceinline__ void load_stage(const Tile& x, int kb, const Params& 
       if (j * 64 < x.nw) l3(sb + j * MN_BOX_BYTES, up ? mB1 : mB0, nb + j * 64, kk, x.e);
   } else {  // wgrad: both operands MN-major, k = token rows of the expert
     const int row = x.lo + k0;
+    const int sh = k_shift<KIND>(x, kb);  // leading rows zero-filled (wgrad tail)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) l2(sa + j * MN_BOX_BYTES, mA, x.m0 + j * 64, row);
+    for (int j = 0; j < 2; ++j) l3(sa + j * MN_BOX_BYTES, mA, x.m0 + j * 64, -sh, row);
 #pragma unroll
-    for (int j = 0; j < B_ROWS / 64; ++j) l2(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, row);
+    for (int j = 0; j < B_ROWS / 64; ++j) l3(sb + j * MN_BOX_BYTES, mB0, nb + j * 64, -sh, row);
   }
 }
 
@@ -638,7 +633,9 @@ __device__ __forceinline__ void epilogue(const Tile& x, const Params& p, uint32_
 // other operand and loads it with TMA.  Forward gate/up: the 128 A rows of a
 // tile (row indices read once per tile).  Gate/up wgrad: the 64 X rows (k)
 // of a k block in each of the four 64-column B boxes (the next block's row
-// indices read before waiting for its stage).  Single-CTA kinds only.  (A
+// indices read before waiting for its stage), shifted like the TMA-loaded
+// dgu rows of an expert's last block (the wgrad tail above), the leading
+// rows zero-filled.  Single-CTA kinds only.  (A
 // tile::gather4 TMA form of the same loads was correct but measured 2.4x
 // slower for the forward and 5x for the wgrad on GB300: it moves 512 bytes
 // per instruction and the TMA unit takes ~40 ns per gather.)
@@ -657,7 +654,6 @@ __device__ __forceinline__ void produce_gathered(const Params& p, const int32_t*
   static_assert(!Traits<KIND>::pair, "gathered operands are single-CTA");
   auto full_bar = [&](int s) { return ctrl + 8u * s; };
   auto empty_bar = [&](int s) { return ctrl + 8u * (STAGES + s); };
-  auto tail_bar = [&](int s) { return ctrl + 8u * (3 * STAGES + 5 + s); };
   const int c = lane & 7, r0 = lane >> 3;  // 16-byte chunk and first row of this lane
   const size_t ld = (size_t)p.g_cols * 2;  // token row bytes
   auto swz = [&](int row) { return (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4); };
@@ -707,11 +703,13 @@ __device__ __forceinline__ void produce_gathered(const Params& p, const int32_t*
       return false;
     };
     bool have = next_tile();
-    int tok[BK / 4];  // token rows of k rows r0 + 4j of the block
+    int tok[BK / 4];  // token rows of box rows r0 + 4j of the block (-1: zero row)
     auto load_rows = [&]() {
-      const int base = x.lo + kb * BK + r0;
+      const int sh = k_shift<KIND>(x, kb);
+      const int base = x.lo + kb * BK + r0 - sh;
 #pragma unroll
-      for (int j = 0; j < BK / 4; ++j) tok[j] = gather_row(p, base + 4 * j, x.hi);
+      for (int j = 0; j < BK / 4; ++j)
+        tok[j] = r0 + 4 * j < sh ? -1 : gather_row(p, base + 4 * j, x.hi);
     };
     if (have) load_rows();
     while (have) {
@@ -722,20 +720,22 @@ __device__ __forceinline__ void produce_gathered(const Params& p, const int32_t*
       const int row = x.lo + kb * BK;
       if (lane == 0) {
         mbar_arrive_expect_tx(full_bar(s), A_BYTES);
+        const int sh = k_shift<KIND>(x, kb);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * MN_BOX_BYTES, mA, full_bar(s), x.m0 + j * 64, row);
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(sa + j * MN_BOX_BYTES, mA, full_bar(s), x.m0 + j * 64, -sh, row);
         issued[s] = (int)ph;
-        if (k_tail<KIND>(x, kb).zl > 0) mbar_arrive(tail_bar(s));
       }
 #pragma unroll
       for (int box = 0; box < Traits<KIND>::b_rows / 64; ++box) {
         const int colx = x.n0 + box * 64 + c * 8;  // columns past H are zero-filled
-        const uint32_t bytes = colx < p.g_cols ? 16u : 0u;
-        const uint8_t* col = p.gsrc + (bytes ? (size_t)colx * 2 : 0);
+        const bool in_cols = colx < p.g_cols;
 #pragma unroll
-        for (int j = 0; j < BK / 4; ++j)
-          cp_async_16(sb + box * MN_BOX_BYTES + swz(r0 + 4 * j), col + (bytes ? (size_t)tok[j] * ld : 0),
-                      bytes);
+        for (int j = 0; j < BK / 4; ++j) {
+          const uint32_t bytes = (in_cols && tok[j] >= 0) ? 16u : 0u;
+          const uint8_t* src = bytes ? p.gsrc + (size_t)colx * 2 + (size_t)tok[j] * ld : p.gsrc;
+          cp_async_16(sb + box * MN_BOX_BYTES + swz(r0 + 4 * j), src, bytes);
+        }
       }
       cp_async_arrive(full_bar(s));
       ++g;
@@ -787,10 +787,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   auto tfull_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return ctrl + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = ctrl + 8u * (2 * STAGES + 4);
-  // wgrad tails: the producer marks a stage whose block has a tail
-  // (tail_bar), the fix warp zeroes it once loaded and releases it (fix_bar)
-  auto fix_bar = [&](int s) { return ctrl + 8u * (2 * STAGES + 5 + s); };
-  auto tail_bar = [&](int s) { return ctrl + 8u * (3 * STAGES + 5 + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gctrl + kHolderOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + kHolderOff + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(gctrl + kPrefixOff);
@@ -816,12 +812,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       mbar_init(tempty_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (Traits<KIND>::wgrad) {
-      for (int s = 0; s < STAGES; ++s) {
-        mbar_init(fix_bar(s), 1);
-        mbar_init(tail_bar(s), 1);
-      }
-    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -902,8 +892,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, fb, &mapA, &mapA64, &mapB0, &mapB1,
                            rank);
           issued[s] = (int)ph;
-          if constexpr (Traits<KIND>::wgrad)
-            if (k_tail<KIND>(x, kb).zl > 0) mbar_arrive(tail_bar(s));
         }
       }
       // Wait for every copy issued before the CTA may exit.  In a pair the
@@ -920,7 +908,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // ---------------- MMA issuer (the leader's, in a pair) ----------------
    if (!PAIR || rank == 0) {
     int g = 0, it = 0;
-    uint32_t fixph = 0;  // bit s: parity of the next fix_bar(s) phase
     bool run = true;
     for (int t = t_first; run && t < wv.slots; t += t_step, ++it) {
       const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
@@ -941,36 +928,26 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
         tc_fence_after();
         const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
-        int nk = BK / UK;
-        if constexpr (Traits<KIND>::wgrad) {
-          // Last k block of an expert: skip whole 16-row groups past its end;
-          // the rest of the last group is zeroed by the fix warp.
-          const KTail kt = k_tail<KIND>(x, kb);
-          nk = kt.nk;
-          if (kt.zl > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(fix_bar(s), (fixph >> s) & 1u, abort_flag, p.status))) {
-              run = false;
-              break;
-            }
-            fixph ^= 1u << s;
-            tc_fence_after();
-          }
-        }
+        // the last k block of an expert in a wgrad: its leading groups of 16
+        // rows are zero-filled (see the wgrad tail) and skipped
+        int kk0 = 0;
+        if constexpr (Traits<KIND>::wgrad) kk0 = k_shift<KIND>(x, kb) / UK;
         // operand rows written by the producer's cp.async (generic proxy),
         // now visible to this thread, made visible to the MMA's reads
         if (gathered) fence_proxy_async_smem();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            if (kk >= nk) break;
+            if (kk < kk0) continue;
             const uint64_t ad = Traits<KIND>::a_mn ? desc_sw128(sa + kk * (UK * 128), MN_BOX_BYTES, 1024)
                                                    : desc_sw128(sa + kk * (UK * 2), 16, 1024);
             const uint64_t bd = Traits<KIND>::b_mn ? desc_sw128(sb + kk * (UK * 128), MN_BOX_BYTES, 1024)
                                                    : desc_sw128(sb + kk * (UK * 2), 16, 1024);
+            const uint32_t accum = (kb > 0 || kk > kk0) ? 1u : 0u;
             if constexpr (PAIR)
               umma_f16_pair(tacc, ad, bd, x.rows < BM ? Traits<KIND>::idesc_half : Traits<KIND>::idesc,
-                            (kb > 0 || kk > 0) ? 1u : 0u);
-            else umma_f16(tacc, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            accum);
+            else umma_f16(tacc, ad, bd, idesc, accum);
           }
           // the stage is free in both CTAs once these MMAs have read it
           if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
@@ -1018,43 +995,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // the CTA's stores must be complete before it exits
     if (lane == 0) bulk_wait_group_all();
     __syncwarp();
-  } else if constexpr (Traits<KIND>::wgrad) {
-    // ---------------- fix warp 10 (wgrads): zero the tail rows ----------------
-    // Visits the tail blocks in the producer's order.  Stage s is refilled
-    // only after the MMA consumed it, which waits for this warp, so each of
-    // tail_bar(s), full_bar(s) and fix_bar(s) is at most one phase ahead.
-    int g = 0;
-    uint32_t tph = 0;  // bit s: parity of the next tail_bar(s) phase
-    bool run = true;
-    for (int t = t_first; run && t < wv.slots; t += t_step) {
-      const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
-      for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
-        const KTail kt = k_tail<KIND>(x, kb);
-        if (kt.zl == 0) continue;
-        const int s = g % STAGES;
-        const uint32_t ph = (g / STAGES) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(tail_bar(s), (tph >> s) & 1u, abort_flag, p.status)) ||
-            !__all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, abort_flag, p.status))) {
-          run = false;
-          break;
-        }
-        tph ^= 1u << s;
-        const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
-        // lane c zeroes 16-byte chunk (c & 7) of tail row z0 + (c >> 3) in
-        // all six operand boxes (2 of A, 4 of B); the rows are 128 bytes and
-        // the 128-byte swizzle only permutes chunks within a row
-        for (int c = lane; c < kt.zl * 8; c += 32) {
-          const uint32_t off = (uint32_t)(kt.z0 + (c >> 3)) * 128u + (uint32_t)(c & 7) * 16u;
-#pragma unroll
-          for (int box = 0; box < 2; ++box) st_shared_v4(sa + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int box = 0; box < 4; ++box) st_shared_v4(sb + box * MN_BOX_BYTES + off, 0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(fix_bar(s));
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1113,6 +1053,26 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, c
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gdim,
                         gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D view of a row-major [rows, cols] bf16 matrix whose dimensions 1 and 2
+// both step one row: element (c, i, j) is row i + j, dimension 1 of extent
+// bk.  The wgrad operands are loaded through it in 64 x bk boxes (128-byte
+// swizzle); a box at (c, i0, j) with i0 < 0 zero-fills its first -i0 rows
+// (see the wgrad tail).  The coordinates used keep every element read
+// inside rows [0, rows).
+bool k_rows_map(CUtensorMap* m, const void* ptr, int cols, int rows, int bk) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t row_bytes = (cuuint64_t)cols * 2;
+  cuuint64_t gdim[3] = {(cuuint64_t)cols, (cuuint64_t)bk, (cuuint64_t)rows};
+  cuuint64_t gstride[2] = {row_bytes, row_bytes};
+  cuuint32_t bdim[3] = {64, (cuuint32_t)bk, 1}, estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim,
+                        gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1193,6 +1153,7 @@ constexpr long long kPairMinRowsGateUpSave = 256;
 constexpr long long kPairMinRowsGateUp = 1024;
 constexpr long long kPairMinRowsDown = 2048;
 constexpr long long kPairMinRowsDgradGateUp = 256;
+constexpr long long kPairMinRowsWgrad = 0;
 inline bool use_pairs(long long min_rows, int N, int E) { return (long long)N >= min_rows * E; }
 
 Params base_params(const int32_t* off, int N, int E, int32_t* status) {
@@ -1369,13 +1330,11 @@ int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H,
 int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, int N, int H,
                            int I, int E, void* dWd, int32_t* status, cudaStream_t s) {
   if (int rc = device_ok()) return rc;
-  const uint32_t box_mn2[2] = {64, (uint32_t)Traits<kWgradDown>::bk};
+  constexpr int BK = Traits<kWgradDown>::bk;
   CUtensorMap m_a, m_b;
-  const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
-  const uint64_t d_a[2] = {(uint64_t)H, rows};
-  const uint64_t d_b[2] = {(uint64_t)I, rows};
-  if (!make_map(&m_a, N > 0 ? dY : dWd, 2, d_a, box_mn2) ||
-      !make_map(&m_b, N > 0 ? act : dWd, 2, d_b, box_mn2))
+  const int rows = N > 0 ? N : 1;
+  if (!k_rows_map(&m_a, N > 0 ? dY : dWd, H, rows, BK) ||
+      !k_rows_map(&m_b, N > 0 ? act : dWd, I, rows, BK))
     return MOE_ERR_CUDA;
   Params p = base_params(off, N, E, status);
   p.I = I;
@@ -1386,7 +1345,9 @@ int launch_down_wgrad_bf16(const void* dY, const void* act, const int32_t* off, 
   p.out = static_cast<__nv_bfloat16*>(dWd);
   CUtensorMap c_dwd;
   if (!store_map_3d(&c_dwd, dWd, I, H, E)) return MOE_ERR_CUDA;
-  return launch<kWgradDown>(m_a, m_a, m_b, m_b, c_dwd, c_dwd, p, s);
+  return use_pairs(kPairMinRowsWgrad, N, E)
+             ? launch<kWgradDown | kPaired>(m_a, m_a, m_b, m_b, c_dwd, c_dwd, p, s)
+             : launch<kWgradDown>(m_a, m_a, m_b, m_b, c_dwd, c_dwd, p, s);
 }
 
 // Gate/up wgrad.  gather == nullptr: X is the permuted [N, H] buffer;
@@ -1395,16 +1356,13 @@ static int gate_up_wgrad_bf16(const void* dgu, const void* X, int T, const int32
                               const int32_t* off, int N, int H, int I, int E, void* dWg,
                               void* dWu, int32_t* status, cudaStream_t s) {
   if (int rc = device_ok()) return rc;
-  const uint32_t box_mn2[2] = {64, (uint32_t)Traits<kWgradGateUp>::bk};
-  const uint32_t box_row[2] = {64, 1};  // (not read when gathering)
+  constexpr int BK = Traits<kWgradGateUp>::bk;
   CUtensorMap m_a, m_b;
-  const uint64_t rows = (uint64_t)(N > 0 ? N : 1);
-  const uint64_t x_rows = gather ? (uint64_t)(T > 0 ? T : 1) : rows;
-  const uint64_t d_a[2] = {(uint64_t)2 * I, rows};
-  const uint64_t d_b[2] = {(uint64_t)H, x_rows};
+  const int rows = N > 0 ? N : 1;
   const bool any = N > 0 && (gather == nullptr || T > 0);
-  if (!make_map(&m_a, any ? dgu : dWg, 2, d_a, box_mn2) ||
-      !make_map(&m_b, any ? X : dWg, 2, d_b, gather ? box_row : box_mn2))
+  // (B is not read through a map when gathering)
+  if (!k_rows_map(&m_a, any ? dgu : dWg, 2 * I, rows, BK) ||
+      !k_rows_map(&m_b, any ? X : dWg, H, gather ? (T > 0 ? T : 1) : rows, BK))
     return MOE_ERR_CUDA;
   Params p = base_params(off, N, E, status);
   p.I = I;
@@ -1422,7 +1380,10 @@ static int gate_up_wgrad_bf16(const void* dgu, const void* X, int T, const int32
   CUtensorMap c_dwg, c_dwu;
   if (!store_map_3d(&c_dwg, dWg, H, I, E) || !store_map_3d(&c_dwu, dWu, H, I, E))
     return MOE_ERR_CUDA;
-  return launch<kWgradGateUp>(m_a, m_a, m_b, m_b, c_dwg, c_dwu, p, s);
+  // gathered X rows are loaded by the single-CTA producer only
+  return (gather == nullptr && use_pairs(kPairMinRowsWgrad, N, E))
+             ? launch<kWgradGateUp | kPaired>(m_a, m_a, m_b, m_b, c_dwg, c_dwu, p, s)
+             : launch<kWgradGateUp>(m_a, m_a, m_b, m_b, c_dwg, c_dwu, p, s);
 }
 
 int launch_gate_up_wgrad_bf16(const void* dgu, const void* X, const int32_t* off, int N, int H,
