@@ -176,14 +176,16 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's sources changed since the capture."""
+def recorded_traffic(workload: str, call: str):
+    """DRAM bytes (read + written) per launch of one call of a workload, from
+    the committed ncu summary (profiles/traffic.json, keyed by workload and
+    call), or None when there is no record or the kernel's sources changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
+        rec = json.load(f).get(workload, {}).get(call)
     if not rec:
         return None
     if source_digest(rec["sources"]) != rec["digest"]:
@@ -635,6 +637,11 @@ def kernel_table(per, work, peaks):
         if by:
             e["gbs"] = by / sec / 1e9
             e["hbm_frac"] = e["gbs"] / peaks["hbm_gbs"]
+        traffic = recorded_traffic(getattr(work, "name", ""), name)
+        if traffic is not None:
+            e["dram_bytes"] = traffic  # ncu, per launch (profiles/traffic.json)
+            if by:
+                e["dram_over_algorithmic"] = traffic / by
         if fl:
             e["tflops"] = fl / sec / 1e12
             e["tensor_frac"] = e["tflops"] / peaks["bf16_tflops_sustained"]
@@ -767,7 +774,7 @@ def run_ours(args, world, rank, local):
     roof["frac"] = achieved / peak
     roof["kernel"] = dom
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback")
-    roof["traffic"] = recorded_traffic(dom)
+    roof["traffic"] = recorded_traffic(work.name, dom)
     roof["algorithmic_bytes"] = work.bytes.get(dom)
     roof["algorithmic_flops"] = work.flops.get(dom)
 

@@ -83,6 +83,26 @@ def test_routing_is_one_launch_when_its_blocks_fit(lib):
     _assert_routing(r, ids, 17)
 
 
+@pytest.mark.parametrize("T,K,E", [(32768, 8, 256), (29127, 9, 1000), (13, 5, 7)])
+def test_routing_one_launch_sizes(lib, T, K, E):
+    """The one-launch routing from 65 to 262143 slots (512 blocks of 512
+    slots), with K that does and does not divide a warp's 32 slots and up to
+    1000 experts."""
+    ids = _ids(T + K, T, K, E)
+    r, launches = _routing_launches(lib, ids, E)
+    assert launches == 1
+    _assert_routing(r, ids, E)
+
+
+def test_routing_one_launch_625_blocks(lib):
+    """320000 slots, 625 blocks of 512 slots, still resident at once: one
+    cooperative launch, bit exact."""
+    ids = _ids(13, 40000, 8, 64)
+    r, launches = _routing_launches(lib, ids, 64)
+    assert launches == 1
+    _assert_routing(r, ids, 64)
+
+
 def test_routing_three_passes_past_residency(lib):
     """2,097,152 slots need 4096 blocks, more than the GPU holds at once: the
     routing falls back to its three launches and stays bit exact."""
@@ -132,6 +152,15 @@ def test_routing_reports_bad_ids(lib):
     ok = lib.new_status()
     lib.moe_permute(None, ids.to(DEV), 16, 0, dev_status=ok)
     assert lib.moe_check_status(ok) == lib.MOE_OK
+    # K = 6 does not divide a 32-slot step: rows straddle steps and warps
+    ids6 = _ids(6, 300, 6, 16)
+    rep6 = ids6.clone()
+    rep6[171, 5] = rep6[171, 0]                # slot 1031 repeats slot 1026 (row 171 spans slots 1026-1031)
+    st = lib.new_status()
+    r = lib.moe_permute(None, rep6.to(DEV), 16, 0, dev_status=st)
+    assert lib.moe_check_status(st) == lib.MOE_ERR_BAD_ID
+    assert int(np64(r.row_map)[171 * 6 + 5]) == -1
+    assert int(np64(r.expert_offsets)[-1]) == 300 * 6 - 1
 
 
 def test_host_rejects_bad_shapes(lib):
