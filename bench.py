@@ -31,7 +31,8 @@ between steps.
 ``e2e`` measures the same steps through the same C-ABI calls with the step's
 inputs copied from pinned host memory and its results copied back inside the
 timed region.  ``cpu_baseline`` times the CPU oracle on a bounded sample of
-the same workload (rank 0, N=1 only).  ``--impl reference`` times the oracle
+the same workload (rank 0, N=1 only), on all host cores and, in a child
+process limited to one thread, on one.  ``--impl reference`` times the oracle
 alone (the reference arm: there is no runnable reference implementation).
 
 Multi-GPU: the layer's token batches are independent, so N GPUs run N
@@ -713,6 +714,30 @@ def time_oracle(work, budget_s: float = 12.0, start_tokens: int = None, max_toke
     return done / spent, cores, f"{n}-token prefix of the same workload, {done // n} run(s), float64 numpy"
 
 
+def time_oracle_single_thread(budget_s: float = 12.0):
+    """The same oracle timing in a child process whose BLAS and OpenMP pools
+    are limited to one thread (the variables must be set before numpy
+    loads).  Returns (tokens/s, sample description), or None if the child
+    failed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", str(budget_s)]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=30 * budget_s)
+        line = [ln for ln in res.stdout.splitlines() if ln.startswith("{")][-1]
+        rec = json.loads(line)
+        return rec["value"], rec["sample"]
+    except Exception:  # noqa: BLE001 - a missing baseline must not fail the bench
+        return None
+
+
+def oracle_child(budget_s: float):
+    """Entry of the single-thread oracle timing (see time_oracle_single_thread)."""
+    work = LayerFwdBwd.host_only(0)
+    v, _, sample = time_oracle(work, budget_s=budget_s, start_tokens=16)
+    print(json.dumps({"value": v, "sample": sample}), flush=True)
+
+
 # ---------------------------------------------------------------- main
 
 def run_ours(args, world, rank, local):
@@ -809,6 +834,10 @@ def run_ours(args, world, rank, local):
         v, cores, sample = time_oracle(work)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
                                   "kind": "oracle", "sample": sample}
+        one = time_oracle_single_thread()
+        if one is not None:
+            result["cpu_baseline"]["single_thread"] = {"value": one[0], "unit": "tokens/s",
+                                                       "cores": 1, "sample": one[1]}
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -925,10 +954,14 @@ def main(argv=None):
     ap.add_argument("--workload", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--oracle-child", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--fused-permute", action="store_true",
                     help="layer workloads: the gate/up GEMMs gather the token rows themselves "
                          "(default: the permute writes the permuted copy they read)")
     args = ap.parse_args(argv)
+    if args.oracle_child is not None:
+        oracle_child(args.oracle_child)
+        return
     if args.fused_permute:
         LayerFwdBwd.FUSED_PERMUTE = True
     if args.warmup < 3 and args.impl == "ours":
