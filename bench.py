@@ -227,7 +227,8 @@ class Timers:
         out = {}
         for name, pairs in self.pending.items():
             ms = [a.elapsed_time(b) for a, b in pairs]
-            out[name] = {"launches": len(ms), "avg_ms": sum(ms) / len(ms), "total_ms": sum(ms)}
+            out[name] = {"launches": len(ms), "avg_ms": sum(ms) / len(ms), "total_ms": sum(ms),
+                         "median_ms": statistics.median(ms)}
         return out
 
 
@@ -634,6 +635,8 @@ def kernel_table(per, work, peaks):
     for name, s in per.items():
         sec = s["avg_ms"] * 1e-3
         e = {"launches": s["launches"], "avg_us": s["avg_ms"] * 1e3, "share": s["total_ms"] / total}
+        if "median_ms" in s:
+            e["median_us"] = s["median_ms"] * 1e3
         by, fl = work.bytes.get(name), work.flops.get(name)
         if by:
             e["gbs"] = by / sec / 1e9
@@ -670,8 +673,10 @@ def measure(work, steps, warmup, sync_barrier=False):
     return t.summary()
 
 
-def run_components(lib, dev, peaks, steps=10, warmup=3):
-    """The other workloads' headline kernels, measured the same way."""
+def run_components(lib, dev, peaks, steps=50, warmup=5):
+    """The other workloads' headline kernels, measured the same way (50
+    steps after 5 warm-up steps; every input is larger than L2, so no flush
+    runs between steps)."""
     comps = {}
     for cls in (PermuteUnpermute, LayerForward, IndexCombine):
         w = cls(lib, dev)
