@@ -195,6 +195,29 @@ def test_bf16_layer_backward(lib, kw):
         assert not np64(g["dWd"][int(e)]).any() and not np64(g["dWg"][int(e)]).any()
 
 
+def test_bf16_layer_backward_zipf_skew(lib):
+    """Zipf(1.2) routing with 8 experts without rows and the largest expert
+    at several hundred rows: the weight-gradient GEMMs' long k loops, their
+    expert tails (partial last k blocks zero-filled by the TMA unit) and
+    the dgrads' skewed tiles, on every row and every expert's weight grads."""
+    d = moe_inputs.layer_forward_zipf(0, T=1024, H=256, E=64, K=8, I=256, num_empty=8)
+    rng = np.random.default_rng(7)
+    d["grad_out"] = torch.from_numpy(rng.standard_normal((d["T"], d["H"])).astype(np.float32)).bfloat16()
+    T, K, E = d["T"], d["K"], d["E"]
+    g = _gpu_layer_fwd_bwd(lib, d)
+    (si, rm, tpe, off), perm, act, expd, _, _ = _oracle_forward(d)
+    assert (tpe == 0).sum() == 8 and tpe.max() > 300 and (tpe % 16 != 0).any()
+    gexp, gprobs = O.unpermute_grad(np64(d["grad_out"]), expd, rm, d["probs"].numpy(), T, K, "bf16")
+    dperm, dWg, dWu, dWd = O.expert_mlp_grad(gexp, perm, act, off, np64(d["W_gate"]),
+                                             np64(d["W_up"]), np64(d["W_down"]), "bf16")
+    N = len(si)
+    assert_normwise(np64(g["dperm"])[:N], dperm, BF16_TOL, "d_permuted")
+    for e in range(E):
+        assert_normwise(np64(g["dWg"][e]), dWg[e], BF16_TOL, f"dW_gate[{e}]")
+        assert_normwise(np64(g["dWu"][e]), dWu[e], BF16_TOL, f"dW_up[{e}]")
+        assert_normwise(np64(g["dWd"][e]), dWd[e], BF16_TOL, f"dW_down[{e}]")
+
+
 def _down_dgrad_last_wave_split(tiles: int, grid: int) -> int:
     """How the single-CTA down projection and dgrads split their last wave
     along N: when the tiles leave a last wave that fills at most half of the
