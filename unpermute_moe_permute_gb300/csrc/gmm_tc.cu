@@ -21,7 +21,9 @@
 //   * gate/up, down and the gate/up dgrad also come as CTA pairs (tcgen05
 //     cta_group::2, a 2-CTA cluster on one TPC, M=256 per MMA, half of the
 //     B tile per CTA, 6-stage ring; an expert's last <= 128 rows as an M=128
-//     half tile), chosen per call and kind from the rows per expert;
+//     half tile), chosen per call and kind from the rows per expert; the two
+//     wgrads always run as pairs (their tiles cover the weight dimensions,
+//     so every pair tile is full);
 //   * the forward gate/up and its wgrad can also read the token matrix
 //     through sorted_indices themselves (the producer warp gathers rows with
 //     cp.async) instead of the permuted copy.
