@@ -907,70 +907,71 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (the leader's, in a pair) ----------------
-   if (!PAIR || rank == 0) {
-    int g = 0, it = 0;
-    bool run = true;
-    for (int t = t_first; run && t < wv.slots; t += t_step, ++it) {
-      const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
-      const uint32_t idesc = x.nw == Traits<KIND>::bn ? Traits<KIND>::idesc
-                                                     : idesc_bf16_f32(BM, x.nw, Traits<KIND>::a_mn,
-                                                                      Traits<KIND>::b_mn);
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u, abort_flag, p.status))) break;
-      tc_fence_after();
-      const uint32_t tacc = tmem_base + acc * Traits<KIND>::bn;
-      for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
-        const int s = g % STAGES;
-        const uint32_t ph = (g / STAGES) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, abort_flag, p.status))) {
-          run = false;
-          break;
-        }
+    // ---------------- MMA issuer: one thread (the leader's, in a pair) ----------------
+    // The tensor pipe is kept fed only if consecutive MMAs are issued with
+    // few instructions between them, so one thread runs this loop alone (no
+    // per-block vote or warp synchronisation), steps the stage and phase
+    // instead of dividing, and forms each MMA's shared-memory descriptors
+    // from per-stage bases and a constant step (the 14-bit address field
+    // cannot carry: shared-memory addresses stay below 2^18 bytes).
+    if ((!PAIR || rank == 0) && lane == 0) {
+      constexpr uint32_t kAStep = Traits<KIND>::a_mn ? (UK * 128) >> 4 : (UK * 2) >> 4;
+      constexpr uint32_t kBStep = Traits<KIND>::b_mn ? (UK * 128) >> 4 : (UK * 2) >> 4;
+      const uint64_t a_desc0 = Traits<KIND>::a_mn ? desc_sw128(sA, MN_BOX_BYTES, 1024) : desc_sw128(sA, 16, 1024);
+      const uint64_t b_desc0 = Traits<KIND>::b_mn ? desc_sw128(sB, MN_BOX_BYTES, 1024) : desc_sw128(sB, 16, 1024);
+      int s = 0, it = 0;
+      uint32_t ph = 0;
+      bool run = true;
+      for (int t = t_first; run && t < wv.slots; t += t_step, ++it) {
+        const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
+        uint32_t idesc;
+        if constexpr (PAIR) idesc = x.rows < BM ? Traits<KIND>::idesc_half : Traits<KIND>::idesc;
+        else idesc = x.nw == Traits<KIND>::bn ? Traits<KIND>::idesc
+                                              : idesc_bf16_f32(BM, x.nw, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t sa = sA + s * A_BYTES, sb = sB + s * B_BYTES;
-        // the last k block of an expert in a wgrad: its leading groups of 16
-        // rows are zero-filled (see the wgrad tail) and skipped
-        int kk0 = 0;
-        if constexpr (Traits<KIND>::wgrad) kk0 = k_shift<KIND>(x, kb) / UK;
-        // operand rows written by the producer's cp.async (generic proxy),
-        // now visible to this thread, made visible to the MMA's reads
-        if (gathered) fence_proxy_async_smem();
-        if (lane == 0) {
+        const uint32_t tacc = tmem_base + acc * Traits<KIND>::bn;
+        uint32_t accum = 0u;  // the tile's first MMA overwrites the accumulator
+        for (int kb = 0; kb < x.kblocks; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
+            run = false;
+            break;
+          }
+          tc_fence_after();
+          // operand rows written by the producer's cp.async (generic proxy),
+          // made visible to the MMA's reads
+          if (gathered) fence_proxy_async_smem();
+          // the last k block of an expert in a wgrad: its leading groups of
+          // 16 rows are zero-filled (see the wgrad tail) and skipped
+          int kk0 = 0;
+          if constexpr (Traits<KIND>::wgrad) kk0 = k_shift<KIND>(x, kb) / UK;
+          const uint64_t ad = a_desc0 + (uint64_t)s * (A_BYTES >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)s * (B_BYTES >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
             if (kk < kk0) continue;
-            const uint64_t ad = Traits<KIND>::a_mn ? desc_sw128(sa + kk * (UK * 128), MN_BOX_BYTES, 1024)
-                                                   : desc_sw128(sa + kk * (UK * 2), 16, 1024);
-            const uint64_t bd = Traits<KIND>::b_mn ? desc_sw128(sb + kk * (UK * 128), MN_BOX_BYTES, 1024)
-                                                   : desc_sw128(sb + kk * (UK * 2), 16, 1024);
-            const uint32_t accum = (kb > 0 || kk > kk0) ? 1u : 0u;
-            if constexpr (PAIR)
-              umma_f16_pair(tacc, ad, bd, x.rows < BM ? Traits<KIND>::idesc_half : Traits<KIND>::idesc,
-                            accum);
-            else umma_f16(tacc, ad, bd, idesc, accum);
+            if constexpr (PAIR) umma_f16_pair(tacc, ad + kk * kAStep, bd + kk * kBStep, idesc, accum);
+            else umma_f16(tacc, ad + kk * kAStep, bd + kk * kBStep, idesc, accum);
+            accum = 1u;
           }
           // the stage is free in both CTAs once these MMAs have read it
           if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
           else umma_commit(empty_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        __syncwarp();
-      }
-      if (!run) break;
-      if (lane == 0) {
+        if (!run) break;
         if constexpr (PAIR) umma_commit_pair(tfull_bar(acc), 3);
         else umma_commit(tfull_bar(acc));
       }
-      __syncwarp();
-    }
-    if (lane == 0) {
       if constexpr (PAIR) umma_commit_pair(drain_bar, 1);
       else umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, abort_flag, p.status, false);
     }
-    __syncwarp();
-   }
   } else if (warp < 2 + kEpiWarps) {
     // ---------------- epilogue warps 2..9 ----------------
     const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
