@@ -864,10 +864,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
                                abort_flag, &mapA, &mapB0, &mapB1);
     }
     if (!gathered && lane == 0) {
-      int issued[kMaxStages];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued[s] = -1;
-      int g = 0;
+      int g = 0, s = 0;  // k blocks issued; stage and phase of the next
+      uint32_t ph = 0;
       bool run = true;
       for (int t = t_first; run && t < wv.slots; t += t_step) {
         const Tile x = decode_slot<KIND>(t, wv, p, prefix, offs, rank);
@@ -877,9 +875,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t tx =
             PAIR ? 2 * (B_BYTES + (x.rows < BM ? A_BYTES / 2 : A_BYTES))
                  : A_BYTES + B_BYTES / Traits<KIND>::bn * (uint32_t)x.nw;
-        for (int kb = 0; kb < x.kblocks; ++kb, ++g) {
-          const int s = g % STAGES;
-          const uint32_t ph = (g / STAGES) & 1;
+        for (int kb = 0; kb < x.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
             run = false;
             break;
@@ -893,17 +889,23 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           }
           load_stage<KIND>(x, kb, p, sA + s * A_BYTES, sB + s * B_BYTES, fb, &mapA, &mapA64, &mapB0, &mapB1,
                            rank);
-          issued[s] = (int)ph;
+          ++g;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
-      // Wait for every copy issued before the CTA may exit.  In a pair the
+      // Wait for every copy issued before the CTA may exit: the last use of
+      // stage st was k block st + S * floor((g - 1 - st) / S).  In a pair the
       // leader's full barriers also count the peer's copies (the peer stays
       // until the closing cluster barrier, which the leader reaches after
       // this wait).
       if (!PAIR || rank == 0) {
-#pragma unroll
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s] >= 0) mbar_wait(full_bar(s), (uint32_t)issued[s], abort_flag, p.status, false);
+        for (int st = 0; st < STAGES && st < g; ++st) {
+          const int last = st + (g - 1 - st) / STAGES * STAGES;
+          mbar_wait(full_bar(st), (uint32_t)(last / STAGES) & 1u, abort_flag, p.status, false);
+        }
       }
     }
   } else if (warp == 1) {
