@@ -1144,18 +1144,22 @@ int device_ok() {
 // Whether a GEMM runs as CTA pairs, from the rows per expert (the routing's
 // skew is not known on the host without a sync).  With half tiles a pair
 // covers the same rows as single CTAs; what remains is how well each kind
-// uses a pair.  GB300, H=2048, bf16, us, pair / single:
-//   routing    rows/    gate/up (I=768|512)   gate/up      down        gate/up
-//              expert   saving (g, u)         not saving               dgrad
-//   uniform      256      196 / 209           188 / 195    108 / 108   189 / 194
-//   uniform      512      310 / 322           301 / 301    170 / 171   305 / 314
-//   uniform     1024      556 / 573           537 / 536    297 / 302   536 / 564
-//   Zipf(1.2)    256      294 / 289           281 / 270    175 / 159   291 / 285
-//   Zipf(1.2)   1024      737 / 778           710 / 723    448 / 440   779 / 806
-// (down at 2048 rows per expert, uniform: 531 / 569; the down dgrad, whose
-// SwiGLU-backward epilogue dominates, measured slower paired everywhere.)
+// uses a pair.  GB300, H=2048, bf16, us, pair / single, with the one-thread
+// MMA issue and the CTA-scope accumulator release:
+//   routing     rows/    gate/up            gate/up      down         gate/up
+//               expert   saving (g, u)      not saving                dgrad
+//   uniform       256    190.7 / 208.8      180.2 / 194.4  105.3 / 108.6  183.3 / 194.7
+//   Zipf(1.2)     256    276.7 / 282.5      264.1 / 262.0  166.0 / 158.6  280.4 / 281.3
+// (gate/up and its dgrad I=768 uniform, I=512 Zipf; the Zipf routing has
+// experts of 22 to 7636 rows, median 72.)  Earlier measurements of the same
+// kinds at 512 and 1024 rows per expert favoured pairs more strongly (for
+// the down projection from 2048 rows, 531 / 569 us); the down projection
+// stays single below that because at 256 rows per expert the skewed routing
+// loses more (+4 %) than the uniform one gains (-3 %).  The down dgrad,
+// whose SwiGLU-backward epilogue dominates, measured slower paired
+// everywhere; the wgrads always run paired.
 constexpr long long kPairMinRowsGateUpSave = 256;
-constexpr long long kPairMinRowsGateUp = 1024;
+constexpr long long kPairMinRowsGateUp = 256;
 constexpr long long kPairMinRowsDown = 2048;
 constexpr long long kPairMinRowsDgradGateUp = 256;
 constexpr long long kPairMinRowsWgrad = 0;
