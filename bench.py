@@ -177,11 +177,11 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, call: str):
-    """DRAM bytes (read + written) per launch of one call of a workload, from
-    the committed ncu summary (profiles/traffic.json, keyed by workload and
-    call), or None when there is no record or the kernel's sources changed
-    since the capture."""
+def recorded_profile(workload: str, call: str):
+    """The committed ncu record of one call of a workload
+    (profiles/traffic.json, keyed by workload and call: DRAM bytes and the
+    kernels' duration per launch), or None when there is no record or the
+    kernel's sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -191,7 +191,14 @@ def recorded_traffic(workload: str, call: str):
         return None
     if source_digest(rec["sources"]) != rec["digest"]:
         return None
-    return rec["bytes_per_launch"]
+    return rec
+
+
+def recorded_traffic(workload: str, call: str):
+    """DRAM bytes (read + written) per launch of one call, from the
+    committed ncu record, or None (see recorded_profile)."""
+    rec = recorded_profile(workload, call)
+    return None if rec is None else rec["bytes_per_launch"]
 
 
 # ---------------------------------------------------------------- workloads
@@ -641,11 +648,16 @@ def kernel_table(per, work, peaks):
         if by:
             e["gbs"] = by / sec / 1e9
             e["hbm_frac"] = e["gbs"] / peaks["hbm_gbs"]
-        traffic = recorded_traffic(getattr(work, "name", ""), name)
-        if traffic is not None:
-            e["dram_bytes"] = traffic  # ncu, per launch (profiles/traffic.json)
+        rec = recorded_profile(getattr(work, "name", ""), name)
+        if rec is not None:
+            # ncu, per launch (profiles/traffic.json): DRAM bytes, and the
+            # kernels' own duration (cold caches, no launch gaps; the event
+            # times above include the gap an event record adds before a call)
+            e["dram_bytes"] = rec["bytes_per_launch"]
+            e["ncu_us"] = rec["ncu_duration_ns"] / 1e3
             if by:
-                e["dram_over_algorithmic"] = traffic / by
+                e["dram_over_algorithmic"] = rec["bytes_per_launch"] / by
+                e["ncu_hbm_frac"] = by / (rec["ncu_duration_ns"] * 1e-9) / 1e9 / peaks["hbm_gbs"]
         if fl:
             e["tflops"] = fl / sec / 1e12
             e["tensor_frac"] = e["tflops"] / peaks["bf16_tflops_sustained"]
