@@ -59,10 +59,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t UNIT_BYTES = 32 * 64;
 constexpr int kMaxStages = 8;
 // control block: 4 * stages + 5 mbarriers, then the TMEM address, the abort
-// flag, the tile prefix and its scan scratch
+// flag, the tile prefix, the staged expert offsets and the scan scratch
 constexpr uint32_t kHolderOff = 8 * (4 * kMaxStages + 5);
 constexpr uint32_t kPrefixOff = kHolderOff + 24;
-constexpr uint32_t CTRL_BYTES = kPrefixOff + 2 * (kMaxExperts + 1) * 4 + 32 * 4;
+constexpr uint32_t ctrl_bytes(int max_experts) {
+  return kPrefixOff + 2 * (uint32_t)(max_experts + 1) * 4 + 32 * 4;
+}
+// Experts a control block sized for few experts holds (kFewExperts below).
+constexpr int kFewMaxExperts = 192;
 
 enum Kind : int {
   kFwdGateUp = 0,
@@ -72,8 +76,11 @@ enum Kind : int {
   kWgradDown = 4,
   kWgradGateUp = 5,
 };
-// A kernel variant is a Kind, plus kPaired for the CTA-pair form.
+// A kernel variant is a Kind, plus kPaired for the CTA-pair form and
+// kFewExperts for a control block sized for at most kFewMaxExperts experts
+// (the shared memory it frees holds another pipeline stage).
 constexpr int kPaired = 8;
+constexpr int kFewExperts = 16;
 constexpr int kind_of(int variant) { return variant & 7; }
 
 template <int KIND>
@@ -110,10 +117,14 @@ struct Traits {
   // ring holding two tiles) lose more to the smaller TMA boxes than they
   // gain from overlap.
   static constexpr int bk = 64;
-  // The SwiGLU-backward epilogue stages two units (dg, du) per piece and is
-  // the slower side of its kernel: it trades a stage for a two-unit ring.
+  // The SwiGLU-backward epilogue stages two units (dg, du) per piece: its
+  // two-unit ring costs a stage unless the control block is sized for few
+  // experts (4 stages and the two-unit ring then fit; measured 133.0 against
+  // 143.9 us with 3 stages at T=4096 K=8 E=128 H=2048 I=768).
   static constexpr int nbuf = kind_of(KIND) == kDgradDown ? 2 : 1;
-  static constexpr int stages = pair ? 6 : (kind_of(KIND) == kDgradDown ? 3 : 4);
+  static constexpr int max_e = (KIND & kFewExperts) ? kFewMaxExperts : kMaxExperts;
+  static constexpr int stages =
+      pair ? 6 : (kind_of(KIND) == kDgradDown && max_e == kMaxExperts ? 3 : 4);
   static_assert(!(pair && kind_of(KIND) == kDgradDown), "the down dgrad runs single-CTA");
   static constexpr uint32_t a_bytes = BM * bk * 2;
   static constexpr uint32_t b_bytes = b_rows * bk * 2;
@@ -121,7 +132,7 @@ struct Traits {
   static constexpr uint32_t mn_box = 64 * bk * 2;  // one 64 (M/N) x bk (K) MN-major box
   static_assert(stages <= kMaxStages, "more stages than the control block holds");
   static constexpr uint32_t staging_bytes = kEpiWarps * nbuf * UNIT_BYTES;
-  static constexpr uint32_t smem_bytes = stages * stage_bytes + staging_bytes + CTRL_BYTES + 1024;
+  static constexpr uint32_t smem_bytes = stages * stage_bytes + staging_bytes + ctrl_bytes(max_e) + 1024;
   static_assert(smem_bytes <= 232448, "more shared memory than one CTA may use");
 };
 
@@ -792,8 +803,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gctrl + kHolderOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + kHolderOff + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(gctrl + kPrefixOff);
-  int32_t* offs = prefix + (kMaxExperts + 1);  // expert offsets, staged once per CTA
-  int32_t* scratch = offs + (kMaxExperts + 1);
+  int32_t* offs = prefix + (Traits<KIND>::max_e + 1);  // expert offsets, staged once per CTA
+  int32_t* scratch = offs + (Traits<KIND>::max_e + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // operand rows gathered from the token matrix by the producer's cp.async
@@ -1299,7 +1310,8 @@ int launch_down_dgrad_bf16(const void* dY, const void* gate_up, const int32_t* o
   p.aux = static_cast<const __nv_bfloat16*>(gate_up);
   CUtensorMap c_dgu;
   if (!store_map_2d(&c_dgu, dgu, 2 * I, N)) return MOE_ERR_CUDA;
-  return launch<kDgradDown>(m_dy, m_dy, m_wd, m_wd, c_dgu, c_dgu, p, s);
+  return E <= kFewMaxExperts ? launch<kDgradDown | kFewExperts>(m_dy, m_dy, m_wd, m_wd, c_dgu, c_dgu, p, s)
+                             : launch<kDgradDown>(m_dy, m_dy, m_wd, m_wd, c_dgu, c_dgu, p, s);
 }
 
 int launch_gate_up_dgrad_bf16(const void* dgu, const int32_t* off, int N, int H, int I, int E,
