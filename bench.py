@@ -403,7 +403,7 @@ class LayerFwdBwd:
                                    f"T={T} H={H} E={E} K={K} I={I} bf16, fp32 probs",
                        "T": T, "H": H, "E": E, "K": K, "I": I, "experts_with_rows": self.E_active,
                        "permute": ("routing only; the gate/up GEMMs gather the token rows "
-                                   "(TMA row gathers)") if self.fused else "routing + row copy",
+                                   "(cp.async row gathers)") if self.fused else "routing + row copy",
                        "l2": "inputs larger than L2 (weights alone exceed it), no flush"}
 
     @classmethod
