@@ -172,7 +172,12 @@ def _gpu_layer_fwd_bwd(lib, d):
 
 
 @pytest.mark.parametrize("kw", SMALL + [dict(T=300, H=192, E=6, K=3, I=320),
-                                  dict(T=200, H=128, E=256, K=4, I=128)])  # many small experts
+                                  dict(T=200, H=128, E=256, K=4, I=128),  # many small experts
+                                  # the down dgrad's four-stage variant (control
+                                  # block for at most 192 experts) and the
+                                  # three-stage one on either side of that bound
+                                  dict(T=500, H=128, E=192, K=6, I=256),
+                                  dict(T=500, H=128, E=193, K=6, I=256)])
 def test_bf16_layer_backward(lib, kw):
     d = moe_inputs.layer_fwd_bwd(2, **kw)
     T, K, E = d["T"], d["K"], d["E"]
