@@ -276,6 +276,11 @@ def _combine_roundings(K):
     (64, 2, 4, 64, 2, 0, 3, False),
     (300, 8, 32, 520, 2, 2, 2, True),     # 65 column vectors: a ragged last lane pass
     (5000, 4, 16, 520, 1, 1, 1, True),    # 625 blocks of 8 tokens
+    # rows split into column runs of whole 32-vector steps, one warp each,
+    # the last run ragged: 2 runs (257 vectors), 3 (385), 4 (513)
+    (300, 8, 32, 2056, 2, 2, 2, True),
+    (129, 6, 24, 3080, 1, 2, 1, True),
+    (70, 8, 32, 4104, 2, 2, 2, False),
 ])
 def test_combine(lib, T, K, E, H, Z, C, Cn, shared):
     d = moe_inputs.index_combine(T + H, R=1, E_local=E, T=T, H=H, K=K, zero_num=Z, copy_num=C,

@@ -23,6 +23,8 @@
 //   combine        x[t] = sum_k scales[t,k] * y(t,k) + shared_x[t] with the
 //                  zero / copy / const expert closed forms of the torch_npu
 //                  npu_moe_distribute_combine_v2 API reference.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -163,19 +165,27 @@ unpermute_grad_kernel(const T* __restrict__ grad_out, const T* __restrict__ X,
 // Kinds of a combine slot.
 enum : int { kRouted = 0, kZero = 1, kCopy = 2, kConst = 3, kBad = 4 };
 
+// The combine splits each token's columns into `parts` runs of whole
+// 32-vector steps, one warp each, in blocks of 4 warps: at H=7168 K=8 this
+// measured 92.4 us against 106.7 for one warp per token in blocks of 8 (the
+// shorter tasks leave less of a partial last wave, and the smaller blocks
+// fit more resident warps at this kernel's register count).
+constexpr int kCombineWarps = 4;
+
 template <typename T, int KMAX>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
                const int32_t* __restrict__ ids, const float* __restrict__ scales,
                const T* __restrict__ shared_x, const T* __restrict__ ori_x,
                const uint8_t* __restrict__ active_mask, int mask_dims, int Tn, int H, int K,
                int N, int E, int zero_num, int copy_num, int const_num, const T* __restrict__ alpha1,
                const T* __restrict__ alpha2, const T* __restrict__ const_v, T* __restrict__ out,
-               int32_t* status) {
+               int32_t* status, int parts) {
   using VT = VecTraits<T>;
   constexpr int EL = VT::kElems;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + warp;
+  const int task = blockIdx.x * kCombineWarps + warp;
+  const int t = task / parts, part = task - t * parts;
   if (t >= Tn) return;
   int my_kind = kBad, my_arg = -1;
   float my_s = 0.f;
@@ -219,8 +229,11 @@ combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
     if (k >= K) kind[k] = kBad;
     need_ori |= (kind[k] == kCopy || kind[k] == kConst);
   }
+  // this warp's columns: vectors [v_lo, v_hi) of the row
   const int nvec = H / EL;
-  for (int v = lane; v < nvec; v += 32) {
+  const int plen = ((nvec + parts - 1) / parts + 31) / 32 * 32;
+  const int v_lo = part * plen, v_hi = min(nvec, v_lo + plen);
+  for (int v = v_lo + lane; v < v_hi; v += 32) {
     const size_t col = (size_t)v * EL;
     // every load of this column chunk is issued before any arithmetic, so an
     // iteration waits for one memory round trip
@@ -289,11 +302,14 @@ void launch_combine(const void* Y, const int32_t* rm, const int32_t* ids, const 
                     const void* sh, const void* ori, const uint8_t* mask, int mask_dims, int Tn,
                     int H, int K, int N, int E, int Z, int C, int Cn, const void* a1,
                     const void* a2, const void* cv, void* out, int32_t* st, cudaStream_t s) {
-  combine_kernel<T, KMAX><<<(Tn + kWarpsPerBlock - 1) / kWarpsPerBlock, 256, 0, s>>>(
+  // column runs per token: up to 4, each at least 128 vectors
+  const int parts = std::max(1, std::min(4, H / VecTraits<T>::kElems / 128));
+  const long long tasks = (long long)Tn * parts;
+  combine_kernel<T, KMAX><<<(unsigned)((tasks + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0, s>>>(
       static_cast<const T*>(Y), rm, ids, sc, static_cast<const T*>(sh),
       static_cast<const T*>(ori), mask, mask_dims, Tn, H, K, N, E, Z, C, Cn,
       static_cast<const T*>(a1),
-      static_cast<const T*>(a2), static_cast<const T*>(cv), static_cast<T*>(out), st);
+      static_cast<const T*>(a2), static_cast<const T*>(cv), static_cast<T*>(out), st, parts);
   count_launches(1);
 }
 
