@@ -122,7 +122,8 @@ int moe_check_status(const int32_t* dev_status, cudaStream_t stream);
  *   row_map         [T*K] int32
  *   tokens_per_expert [E] int32, expert_offsets [E+1] int32
  *   workspace       device scratch of moe_permute_workspace_size(T, K, E)
- *                   bytes: ceil(T*K/512) blocks of E int32 expert counts
+ *                   bytes, 16-byte aligned (else MOE_ERR_INVALID_ARG):
+ *                   ceil(T*K/512) blocks of E int32 expert counts
  *                   (padded to 8 bytes), then one 8-byte completion flag
  *                   per block.  Its contents need no clearing: each call
  *                   stamps the flags with a value no earlier call of the

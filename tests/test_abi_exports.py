@@ -89,6 +89,7 @@ HOST_CHECKS = [
     ("moe_combine_masked", (P, BF16, P, P, P, None, None, P, 3, 4, 64, 2, 8, 8, 0, 0, 0, None, None, None, P, None, None), INV),  # mask_dims 3
     ("moe_permute_masked", (P, BF16, P, 4, 64, 2, 8, 0, P, 0, P, P, P, P, P, P, 1 << 20, None, None), INV),  # mask_dims 0
     ("moe_permute", (P, BF16, P, 4, 64, 2, 8, 0, P, P, P, P, P, P, 0, None, None), INV),         # workspace too small
+    ("moe_permute", (P, BF16, P, 4, 64, 2, 8, 0, P, P, P, P, P, U, 1 << 20, None, None), INV),   # workspace unaligned
     ("moe_permute", (P, BF16, P, 4, 64, 4, 2, 1, P, P, P, P, P, P, 1 << 20, None, None), SHAPE),  # K > E + specials
     ("moe_permute_static_scratch", (P, BF16, P, 1 << 20, 64, 8, 1024, 0, P, P, P, P, P, None, None), CAP),  # scratch too small
     ("moe_invert_sorted_indices", (P, 10, 8, P, None), INV),                                     # N > T*K

@@ -59,6 +59,25 @@ def test_routing_bit_exact(lib, T, K, E, special):
     _routing_check(lib, _ids(T + K + E, T, K, E + special), E, special)
 
 
+@pytest.mark.parametrize("E", [64, 17])
+def test_routing_workspace_alignment(lib, E):
+    """The routing's per-block counts are read 16 bytes at a time when E is
+    a multiple of 4 (one count at a time otherwise) and its flags are
+    8-byte words, so the workspace must be 16-byte aligned: a workspace 4
+    bytes past a 16-byte boundary is refused on the host, before any launch,
+    and an aligned one gives the oracle's routing bit for bit."""
+    T, K = 2049, 8
+    ids = _ids(5, T, K, E)
+    size = lib.moe_permute_workspace_size(T, K, E)
+    base = torch.zeros(size + 16, dtype=torch.uint8, device=DEV)
+    assert base.data_ptr() % 16 == 0
+    with pytest.raises(lib.MoeError) as err:
+        lib.moe_permute(None, ids.to(DEV), E, 0, workspace=base[4: 4 + size])
+    assert err.value.status == lib.MOE_ERR_INVALID_ARG
+    r = lib.moe_permute(None, ids.to(DEV), E, 0, workspace=base[:size])
+    _assert_routing(r, ids, E)
+
+
 def _routing_launches(lib, ids_cpu, E):
     before = lib.moe_kernel_launches()
     r = lib.moe_permute(None, ids_cpu.to(DEV), E, 0)
