@@ -8,7 +8,9 @@
 //     (expert, m-tile, n-tile) tiles computed on the device from the expert
 //     row offsets (no host sync, empty experts have no tiles);
 //   * warp 0 issues TMA loads of 128x64 A and 256x64 B bf16 tiles (128-byte
-//     swizzle) into a 4-stage shared-memory ring;
+//     swizzle) into a 4-stage shared-memory ring (the down dgrad, whose
+//     epilogue stages two units per piece, has 4 stages only with its
+//     control block sized for at most 192 experts, else 3);
 //   * warp 1 allocates 512 tensor-memory columns (two 128x256 fp32
 //     accumulators) and one thread issues tcgen05.mma (M=128, N=256, K=16);
 //   * warps 2-9 (two per TMEM lane quarter, each taking half of the
