@@ -167,7 +167,7 @@ enum : int { kRouted = 0, kZero = 1, kCopy = 2, kConst = 3, kBad = 4 };
 
 // The combine splits each token's columns into `parts` runs of whole
 // 32-vector steps, one warp each, in blocks of 4 warps: at H=7168 K=8 this
-// measured 92.4 us against 106.7 for one warp per token in blocks of 8 (the
+// measured 93.3 us against 106.7 for one warp per token in blocks of 8 (the
 // shorter tasks leave less of a partial last wave, and the smaller blocks
 // fit more resident warps at this kernel's register count).
 constexpr int kCombineWarps = 4;
@@ -184,8 +184,8 @@ combine_kernel(const T* __restrict__ Y, const int32_t* __restrict__ row_map,
   using VT = VecTraits<T>;
   constexpr int EL = VT::kElems;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int task = blockIdx.x * kCombineWarps + warp;
-  const int t = task / parts, part = task - t * parts;
+  const long long task = (long long)blockIdx.x * kCombineWarps + warp;
+  const int t = (int)(task / parts), part = (int)(task - (long long)t * parts);
   if (t >= Tn) return;
   int my_kind = kBad, my_arg = -1;
   float my_s = 0.f;
