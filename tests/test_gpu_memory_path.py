@@ -153,6 +153,32 @@ def test_routing_empty_and_all_special(lib):
     assert off[-1] == 0 and np.all(np64(r.row_map) == -1)
 
 
+def test_empty_token_batches(lib):
+    """T = 0 through every memory-bound entry point: each returns MOE_OK,
+    writes nothing and reads nothing (empty buffers, counts all zero)."""
+    H, K, E = 64, 4, 8
+    bf = torch.bfloat16
+    tok = torch.empty((0, H), dtype=bf, device=DEV)
+    ids = torch.empty((0, K), dtype=torch.int32, device=DEV)
+    r = lib.moe_permute(tok, ids, E, 0)
+    assert r.permuted.shape[0] == 0 and not np64(r.tokens_per_expert).any()
+    assert not np64(r.expert_offsets).any()
+    rm = torch.empty(0, dtype=torch.int32, device=DEV)
+    probs = torch.empty((0, K), dtype=torch.float32, device=DEV)
+    rows = torch.empty((0, H), dtype=bf, device=DEV)
+    assert lib.moe_unpermute(rows, rm, probs, 0, K).shape == (0, H)
+    assert lib.moe_permute_grad(rows, rm, 0, K).shape == (0, H)
+    gp, gprobs = lib.moe_unpermute_grad(tok, rows, rm, probs, K)
+    assert gp.shape == (0, H) and gprobs.shape == (0, K)
+    assert lib.moe_permute_rows(tok, rm, K, 0).shape == (0, H)
+    out = lib.moe_combine(rows, rm, ids, probs, E)
+    assert out.shape == (0, H)
+    # counts all zero: no index, every expert empty, total 0
+    counts = torch.zeros(4 * E, dtype=torch.int32, device=DEV)
+    _, tpe, total = lib.moe_permute_indices(counts, 4, E, 16)
+    assert int(total.item()) == 0 and not np64(tpe).any()
+
+
 def test_routing_reports_bad_ids(lib):
     ids = _ids(5, 64, 4, 16)
     bad_range = ids.clone()
