@@ -104,9 +104,9 @@ def test_routing_is_one_launch_when_its_blocks_fit(lib):
 
 @pytest.mark.parametrize("T,K,E", [(32768, 8, 256), (29127, 9, 1000), (13, 5, 7)])
 def test_routing_one_launch_sizes(lib, T, K, E):
-    """The one-launch routing from 65 to 262143 slots (512 blocks of 512
-    slots), with K that does and does not divide a warp's 32 slots and up to
-    1000 experts."""
+    """The one-launch routing from 65 to 262143 slots (blocks of 512 slots up
+    to 64 blocks, of 1024 slots past that: up to 256 blocks), with K that
+    does and does not divide a warp's 32 slots and up to 1000 experts."""
     ids = _ids(T + K, T, K, E)
     r, launches = _routing_launches(lib, ids, E)
     assert launches == 1
@@ -114,7 +114,7 @@ def test_routing_one_launch_sizes(lib, T, K, E):
 
 
 def test_routing_one_launch_625_blocks(lib):
-    """320000 slots, 625 blocks of 512 slots, still resident at once: one
+    """320000 slots, 313 blocks of 1024 slots, resident at once: one
     cooperative launch, bit exact."""
     ids = _ids(13, 40000, 8, 64)
     r, launches = _routing_launches(lib, ids, 64)
@@ -123,8 +123,9 @@ def test_routing_one_launch_625_blocks(lib):
 
 
 def test_routing_three_passes_past_residency(lib):
-    """2,097,152 slots need 4096 blocks, more than the GPU holds at once: the
-    routing falls back to its three launches and stays bit exact."""
+    """2,097,152 slots need 2048 blocks of 1024 slots, more than the GPU
+    holds at once: the routing falls back to its three launches (blocks of
+    512 slots) and stays bit exact."""
     ids = _ids(12, 262144, 8, 64)
     r, launches = _routing_launches(lib, ids, 64)
     assert launches == 3

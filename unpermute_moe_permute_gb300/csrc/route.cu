@@ -232,6 +232,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 constexpr unsigned long long kFlagWaitNs = 2000000000ull;  // 2 s
 
+template <int kSteps>
 __global__ void __launch_bounds__(kRouteThreads)
 route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_total, SlotMask m,
                    int32_t* __restrict__ blk_counts, unsigned long long* __restrict__ flags,
@@ -252,9 +253,9 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
   if (tid == 0) timed_out = 0;
   __syncthreads();
   // 1. experts of this warp's 64 slots (kept for phase 5) and warp counts
-  const int wbase = b * kChunk + warp * kSlotsPerWarp;
+  constexpr int kWarpSlots = 32 * kSteps, kBlockSlots = kRouteWarps * kWarpSlots;
+  const int wbase = b * kBlockSlots + warp * kWarpSlots;
   int32_t* my = cnt + warp * E;
-  constexpr int kSteps = kSlotsPerWarp / 32;
   int ex[kSteps];
   bool any_bad = false;
 #pragma unroll
@@ -299,7 +300,8 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
     // Leave no stale entry behind: this block's slots are not dispatched
     // (the row copy skips them), and block 0 publishes an empty routing.
     if (tid == 0) set_status(status, MOE_ERR_TIMEOUT);
-    for (int f = b * kChunk + tid; f < min((b + 1) * kChunk, TK); f += kRouteThreads) row_map[f] = -1;
+    for (int f = b * kBlockSlots + tid; f < min((b + 1) * kBlockSlots, TK); f += kRouteThreads)
+      row_map[f] = -1;
     if (b == 0) {
       for (int e = tid; e < E; e += kRouteThreads) tokens_per_expert[e] = 0;
       for (int e = tid; e <= E; e += kRouteThreads) expert_offsets[e] = 0;
@@ -488,7 +490,8 @@ static inline size_t flags_offset(long long nblk, int E) {
 static inline size_t fused_smem_bytes(int E) { return (size_t)(kRouteWarps + 2) * E * sizeof(int32_t); }
 
 // Whether nblk blocks of the fused routing kernel fit on the current device
-// at once (cooperative launch); cached per (device, E).
+// at once (cooperative launch); cached per (kernel, device, E).
+template <int kSteps>
 static bool fused_fits(int nblk, int E) {
   static std::mutex mu;
   static std::map<std::pair<int, int>, int> cap;  // (device, E) -> resident blocks
@@ -500,14 +503,16 @@ static bool fused_fits(int nblk, int E) {
     int coop = 0, per_sm = 0;
     int n = 0;
     if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_fused_kernel, kRouteThreads,
-                                                      fused_smem_bytes(E)) == cudaSuccess)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_fused_kernel<kSteps>,
+                                                      kRouteThreads, fused_smem_bytes(E)) ==
+            cudaSuccess)
       n = per_sm * sm_count();
     (void)cudaGetLastError();
     it = cap.emplace(std::make_pair(dev, E), n).first;
   }
   return nblk <= it->second;
 }
+
 
 // splitmix64 finaliser (Steele, Lea, Flood, "Fast splittable pseudorandom
 // number generators", OOPSLA 2014): spreads every input bit over the output.
@@ -540,6 +545,35 @@ static unsigned long long next_stamp() {
     v = counter.fetch_add(1ull);
   } while (v == 0ull);
   return v;
+}
+
+// One cooperative launch of the fused routing with kSteps 32-slot steps per
+// warp; false if its blocks do not all fit at once or the launch fails.
+template <int kSteps>
+static bool launch_route_fused(const int32_t* expert_ids, int TK, int K, int E, int E_total,
+                               SlotMask m, void* workspace, int32_t* sorted_indices,
+                               int32_t* row_map, int32_t* tokens_per_expert,
+                               int32_t* expert_offsets, int32_t* dev_status,
+                               cudaStream_t stream) {
+  constexpr int kBlockSlots = kRouteWarps * 32 * kSteps;
+  const int nblk = (TK + kBlockSlots - 1) / kBlockSlots;
+  if (!fused_fits<kSteps>(nblk, E)) return false;
+  int32_t* blk = static_cast<int32_t*>(workspace);
+  unsigned long long* flags =
+      reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + flags_offset(nblk, E));
+  unsigned long long stamp = next_stamp();
+  void* args[] = {(void*)&expert_ids, (void*)&TK, (void*)&K, (void*)&E, (void*)&E_total,
+                  (void*)&m, (void*)&blk, (void*)&flags, (void*)&stamp, (void*)&sorted_indices,
+                  (void*)&row_map, (void*)&tokens_per_expert, (void*)&expert_offsets,
+                  (void*)&dev_status};
+  if (cudaLaunchCooperativeKernel((const void*)route_fused_kernel<kSteps>, dim3(nblk),
+                                  dim3(kRouteThreads), args, fused_smem_bytes(E), stream) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  count_launches(1);
+  return true;
 }
 
 }  // namespace moe
@@ -591,24 +625,17 @@ extern "C" int moe_permute_masked(const void* tokens, int dtype, const int32_t* 
   int32_t* blk = static_cast<int32_t*>(workspace);
   const int E_total = E + num_special;
   const SlotMask m{active_mask, mask_dims};
-  bool fused = false;
-  if (fused_fits(nblk, E)) {
-    // all blocks resident: the three routing passes as one launch
-    unsigned long long* flags =
-        reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + flags_offset(nblk, E));
-    unsigned long long stamp = next_stamp();
-    void* args[] = {(void*)&expert_ids, (void*)&TK, (void*)&K, (void*)&E, (void*)&E_total,
-                    (void*)&m, (void*)&blk, (void*)&flags, (void*)&stamp, (void*)&sorted_indices,
-                    (void*)&row_map, (void*)&tokens_per_expert, (void*)&expert_offsets,
-                    (void*)&dev_status};
-    if (cudaLaunchCooperativeKernel((const void*)route_fused_kernel, dim3(nblk), dim3(kRouteThreads),
-                                    args, fused_smem_bytes(E), stream) == cudaSuccess) {
-      fused = true;
-      count_launches(1);
-    } else {
-      (void)cudaGetLastError();
-    }
-  }
+  // All blocks resident: the three routing passes as one launch.  Each
+  // block reads every block's counts, so past 64 blocks of 512 slots the
+  // blocks take 1024 slots (T=8192 K=8 E=256: 16.7 -> 12.5 us; at 64 or
+  // fewer blocks the 512-slot blocks measured faster).  The workspace is
+  // sized for 512-slot blocks, which covers both layouts.
+  const bool fused =
+      TK > 64 * kChunk
+          ? launch_route_fused<4>(expert_ids, TK, K, E, E_total, m, workspace, sorted_indices,
+                                  row_map, tokens_per_expert, expert_offsets, dev_status, stream)
+          : launch_route_fused<2>(expert_ids, TK, K, E, E_total, m, workspace, sorted_indices,
+                                  row_map, tokens_per_expert, expert_offsets, dev_status, stream);
   if (!fused) {
     route_hist_kernel<<<nblk, kRouteThreads, E * sizeof(int32_t), stream>>>(
         expert_ids, TK, K, E, E_total, m, blk, dev_status);
