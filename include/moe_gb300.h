@@ -125,7 +125,9 @@ int moe_check_status(const int32_t* dev_status, cudaStream_t stream);
  *                   bytes, 16-byte aligned (else MOE_ERR_INVALID_ARG):
  *                   ceil(T*K/512) blocks of E int32 expert counts
  *                   (padded to 8 bytes), then one 8-byte completion flag
- *                   per block.  Its contents need no clearing: each call
+ *                   per block (a routing with more than 64 such blocks
+ *                   uses half as many blocks of 1024 slots, in the same
+ *                   bytes).  Its contents need no clearing: each call
  *                   stamps the flags with a value no earlier call of the
  *                   process used (seeded from the clock, the process id and
  *                   a random draw, so a stamp left by another process
