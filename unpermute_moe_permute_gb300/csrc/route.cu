@@ -252,7 +252,8 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
   for (int i = tid; i < (kRouteWarps + 2) * E; i += kRouteThreads) sm[i] = 0;
   if (tid == 0) timed_out = 0;
   __syncthreads();
-  // 1. experts of this warp's 64 slots (kept for phase 5) and warp counts
+  // 1. experts of this warp's 32 * kSteps slots (kept for phase 7) and warp
+  //    counts
   constexpr int kWarpSlots = 32 * kSteps, kBlockSlots = kRouteWarps * kWarpSlots;
   const int wbase = b * kBlockSlots + warp * kWarpSlots;
   int32_t* my = cnt + warp * E;
@@ -423,9 +424,10 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
 // (kRowUnroll = 16: a 4 KB row in one round of loads) and writes with
 // streaming stores, since the permuted rows are not re-read here: at
 // T=4096 H=2048 K=8 this measured 35.9 us against 40.9 with 4 vectors and
-// plain stores (routing included), 202.7 against 210.7 at T=16384 H=4096.  Slots whose row lies outside [0, N) (N = rows of
-// the permuted buffer) are skipped: -1 marks a slot that is not dispatched,
-// and nothing else may address memory outside the buffer.
+// plain stores (routing included), 202.7 against 210.7 at T=16384 H=4096.
+// Slots whose row lies outside [0, N) (N = rows of the permuted buffer) are
+// skipped: -1 marks a slot that is not dispatched, and nothing else may
+// address memory outside the buffer.
 template <int kUnroll>
 __global__ void __launch_bounds__(256)
 permute_rows_kernel(const uint8_t* __restrict__ tokens, const int32_t* __restrict__ row_map, int T,
@@ -512,7 +514,6 @@ static bool fused_fits(int nblk, int E) {
   }
   return nblk <= it->second;
 }
-
 
 // splitmix64 finaliser (Steele, Lea, Flood, "Fast splittable pseudorandom
 // number generators", OOPSLA 2014): spreads every input bit over the output.
